@@ -1,0 +1,232 @@
+"""Float64 CPU oracle of the contrastive scoring path (TEST INFRASTRUCTURE ONLY).
+
+Only `tests/`, `__graft_entry__.smoke()` and `bench.py`'s CPU-baseline leg (and
+its `--impl reference` arm) may import this package.  The product path never
+does: it shares no code with the CUDA library and is not a fallback for it.
+
+The arithmetic lives in `cli_oracle.c` (plain C, float64); this module builds
+it with gcc on first use and marshals numpy arrays through ctypes.
+
+Pins: every function is checked by `tests/test_oracle.py` against closed
+forms, brute force, finite differences and invariants; nothing here is
+"parity unpinned".
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "cli_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libcli_oracle.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (float64, no fast-math) into oracle/_build/."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-fno-fast-math",
+                        "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I64, D, I = ctypes.c_int64, ctypes.c_double, ctypes.c_int
+            lib.oracle_sigmoid.argtypes = [D]
+            lib.oracle_sigmoid.restype = D
+            lib.oracle_softplus.argtypes = [D]
+            lib.oracle_softplus.restype = D
+            lib.oracle_pair_loss_sigmoid.argtypes = [I64, I64, P, D, D, P, P, P, P, P, P, P, P, I, D,
+                                                     I64, P, P, P, P, P, P, I]
+            lib.oracle_pair_loss_sigmoid_scores.argtypes = [I64, I64, P, D, D, P, P, P, P, P, P, P, P, P,
+                                                            I, D, P, P, P, P]
+            lib.oracle_maxsim_pairs.argtypes = [I64, P, P, I64, P, P, I64, I, I64, P, P, P, P, P, P, I]
+            lib.oracle_maxsim_forward.argtypes = [I64, P, P, I64, P, P, I64, I, P, P, P, I]
+            lib.oracle_maxsim_backward.argtypes = [I64, P, P, I64, P, P, I64, I, P, P, P, P, I]
+            lib.oracle_maxsim_grad_query.argtypes = [I64, P, P, I64, P, P, I64, I, I64, P, P]
+            lib.oracle_maxsim_grad_doc.argtypes = [I64, P, P, I64, P, P, I64, I, I64, P, P]
+            for f in ("oracle_pair_loss_sigmoid", "oracle_pair_loss_sigmoid_scores", "oracle_maxsim_pairs",
+                      "oracle_maxsim_forward", "oracle_maxsim_backward", "oracle_maxsim_grad_query",
+                      "oracle_maxsim_grad_doc"):
+                getattr(lib, f).restype = I
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f64(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _u64(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.uint64)
+
+
+def _u32(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.uint32)
+
+
+def sigmoid(x: float) -> float:
+    return _load().oracle_sigmoid(float(x))
+
+
+def softplus(x: float) -> float:
+    return _load().oracle_softplus(float(x))
+
+
+def _edges(e):
+    """(offsets, ids, weights) from an Edges-like object, a tuple, or None."""
+    if e is None:
+        return None, None, None
+    if isinstance(e, tuple):
+        off, ids = e[0], e[1]
+        w = e[2] if len(e) > 2 else None
+    else:
+        off, ids, w = e.offsets, e.ids, e.weights
+    if off is None:
+        return None, None, None
+    return _u64(off), _u32(ids if len(ids) else np.zeros(1, np.uint32)), _f64(w)
+
+
+def pair_loss_sigmoid(e, t, b, attract=None, repel=None, ignore=None, negatives_named=False,
+                      ambient_weight=1.0, rows=None, want_de=True, threads=None):
+    """Pooled sigmoid pair loss.  Returns dict(loss, dt, db, de, row_loss).
+
+    With `rows`, only those anchors are evaluated: `loss`, `dt`, `db` are their
+    shares and `de`/`row_loss` have one entry per listed anchor.
+    """
+    lib = _load()
+    e = _f64(e)
+    n, w = e.shape
+    ao, ai, aw = _edges(attract)
+    ro, ri, rw = _edges(repel)
+    io, ii, _ = _edges(ignore)
+    sel = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    m = n if sel is None else len(sel)
+    de = np.zeros((m, w)) if want_de else None
+    row_loss = np.zeros(m)
+    out = np.zeros(3)
+    rc = lib.oracle_pair_loss_sigmoid(n, w, _ptr(e), float(t), float(b), _ptr(ao), _ptr(ai), _ptr(aw),
+                                      _ptr(ro), _ptr(ri), _ptr(rw), _ptr(io), _ptr(ii), int(negatives_named),
+                                      float(ambient_weight), m, _ptr(sel), _ptr(out[0:1]), _ptr(de),
+                                      _ptr(row_loss), _ptr(out[1:2]), _ptr(out[2:3]),
+                                      threads or default_threads())
+    assert rc == 0
+    return dict(loss=out[0], dt=out[1], db=out[2], de=de, row_loss=row_loss)
+
+
+def pair_loss_sigmoid_scores(scores, t, b, attract=None, repel=None, ignore=None, sides=None,
+                             negatives_named=False, ambient_weight=1.0):
+    """Sigmoid pair loss over a given score matrix [R, C].  Returns dict(loss, dt, db, dscores)."""
+    lib = _load()
+    s = _f64(scores)
+    r, c = s.shape
+    ao, ai, aw = _edges(attract)
+    ro, ri, rw = _edges(repel)
+    io, ii, _ = _edges(ignore)
+    sd = None if sides is None else np.ascontiguousarray(sides, dtype=np.uint8)
+    ds = np.zeros((r, c))
+    out = np.zeros(3)
+    rc = lib.oracle_pair_loss_sigmoid_scores(r, c, _ptr(s), float(t), float(b), _ptr(ao), _ptr(ai), _ptr(aw),
+                                             _ptr(ro), _ptr(ri), _ptr(rw), _ptr(io), _ptr(ii), _ptr(sd),
+                                             int(negatives_named), float(ambient_weight), _ptr(out[0:1]),
+                                             _ptr(ds), _ptr(out[1:2]), _ptr(out[2:3]))
+    assert rc == 0
+    return dict(loss=out[0], dt=out[1], db=out[2], dscores=ds)
+
+
+def maxsim_forward(q_off, q, d_off, d, mean=False, threads=None):
+    """All pairs.  Returns (scores [nq, nd], argmax [nd, rows_q] int32, gap [nd, rows_q])."""
+    lib = _load()
+    q_off, d_off, q, d = _u64(q_off), _u64(d_off), _f64(q), _f64(d)
+    nq, nd, w = len(q_off) - 1, len(d_off) - 1, q.shape[1]
+    rows_q = int(q_off[-1])
+    scores = np.zeros((nq, nd))
+    argmax = np.zeros((nd, rows_q), dtype=np.int32)
+    gap = np.zeros((nd, rows_q))
+    rc = lib.oracle_maxsim_forward(nq, _ptr(q_off), _ptr(q), nd, _ptr(d_off), _ptr(d), w, int(mean),
+                                   _ptr(scores), _ptr(argmax), _ptr(gap), threads or default_threads())
+    assert rc == 0
+    return scores, argmax, gap
+
+
+def maxsim_pairs(q_off, q, d_off, d, pairs_q, pairs_d, mean=False, threads=None):
+    """Listed pairs.  Returns (scores [P], argmax list, gap list) with one |q|-array per pair."""
+    lib = _load()
+    q_off, d_off, q, d = _u64(q_off), _u64(d_off), _f64(q), _f64(d)
+    nq, nd, w = len(q_off) - 1, len(d_off) - 1, q.shape[1]
+    pq = np.ascontiguousarray(pairs_q, dtype=np.int64)
+    pd = np.ascontiguousarray(pairs_d, dtype=np.int64)
+    lens = (q_off[pq + 1] - q_off[pq]).astype(np.int64)
+    arg_off = np.zeros(len(pq) + 1, dtype=np.int64)
+    arg_off[1:] = np.cumsum(lens)
+    score = np.zeros(len(pq))
+    argmax = np.zeros(int(arg_off[-1]), dtype=np.int32)
+    gap = np.zeros(int(arg_off[-1]))
+    rc = lib.oracle_maxsim_pairs(nq, _ptr(q_off), _ptr(q), nd, _ptr(d_off), _ptr(d), w, int(mean), len(pq),
+                                 _ptr(pq), _ptr(pd), _ptr(arg_off), _ptr(score), _ptr(argmax), _ptr(gap),
+                                 threads or default_threads())
+    assert rc == 0
+    return (score, [argmax[arg_off[k]:arg_off[k + 1]] for k in range(len(pq))],
+            [gap[arg_off[k]:arg_off[k + 1]] for k in range(len(pq))])
+
+
+def maxsim_backward(q_off, q, d_off, d, argmax, dscores, mean=False, threads=None):
+    """Returns (dq [rows_q, W], dd [rows_d, W]) given the oracle's argmax [nd, rows_q]."""
+    lib = _load()
+    q_off, d_off, q, d = _u64(q_off), _u64(d_off), _f64(q), _f64(d)
+    nq, nd, w = len(q_off) - 1, len(d_off) - 1, q.shape[1]
+    am = np.ascontiguousarray(argmax, dtype=np.int32)
+    ds = _f64(dscores)
+    dq = np.zeros((int(q_off[-1]), w))
+    dd = np.zeros((int(d_off[-1]), w))
+    rc = lib.oracle_maxsim_backward(nq, _ptr(q_off), _ptr(q), nd, _ptr(d_off), _ptr(d), w, int(mean), _ptr(am),
+                                    _ptr(ds), _ptr(dq), _ptr(dd), threads or default_threads())
+    assert rc == 0
+    return dq, dd
+
+
+def maxsim_grad_query(q_off, q, d_off, d, qi, dscores_row, mean=False):
+    """dQ rows of query `qi` (its own argmax computed inside)."""
+    lib = _load()
+    q_off, d_off, q, d = _u64(q_off), _u64(d_off), _f64(q), _f64(d)
+    nq, nd, w = len(q_off) - 1, len(d_off) - 1, q.shape[1]
+    out = np.zeros((int(q_off[qi + 1] - q_off[qi]), w))
+    rc = lib.oracle_maxsim_grad_query(nq, _ptr(q_off), _ptr(q), nd, _ptr(d_off), _ptr(d), w, int(mean), int(qi),
+                                      _ptr(_f64(dscores_row)), _ptr(out))
+    assert rc == 0
+    return out
+
+
+def maxsim_grad_doc(q_off, q, d_off, d, di, dscores_col, mean=False):
+    """dD rows of document `di` (its own argmax computed inside)."""
+    lib = _load()
+    q_off, d_off, q, d = _u64(q_off), _u64(d_off), _f64(q), _f64(d)
+    nq, nd, w = len(q_off) - 1, len(d_off) - 1, q.shape[1]
+    out = np.zeros((int(d_off[di + 1] - d_off[di]), w))
+    rc = lib.oracle_maxsim_grad_doc(nq, _ptr(q_off), _ptr(q), nd, _ptr(d_off), _ptr(d), w, int(mean), int(di),
+                                    _ptr(_f64(dscores_col)), _ptr(out))
+    assert rc == 0
+    return out
