@@ -1,0 +1,445 @@
+// The C ABI of include/cli.h: host-side argument checks, workspace carve-up,
+// TMA descriptors and kernel launches.  Nothing here allocates device memory.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <cmath>
+
+#include "../../include/cli.h"
+#include "cli_internal.h"
+
+namespace cli {
+namespace {
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+Range range_of(const void *p, size_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return {a, a + bytes};
+}
+
+bool overlaps(const Range &a, const Range &b) {
+    if (a.lo == a.hi || b.lo == b.hi || a.lo == 0 || b.lo == 0) return false;
+    return a.lo < b.hi && b.lo < a.hi;
+}
+
+// True when any output range overlaps any input range or another output.
+bool any_overlap(const Range *in, int nin, const Range *out, int nout) {
+    for (int o = 0; o < nout; ++o) {
+        for (int i = 0; i < nin; ++i)
+            if (overlaps(out[o], in[i])) return true;
+        for (int p = o + 1; p < nout; ++p)
+            if (overlaps(out[o], out[p])) return true;
+    }
+    return false;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// bf16 [rows x cols] with row stride ld (elements), boxes of 64 x 128 with the
+// 128-byte swizzle; out-of-range elements read as zero.
+bool encode_bf16_rows(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t ld) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+bool edges_ok(const cli_edges_t &e) {
+    if (!e.offsets) return e.edges == 0;
+    if (e.edges > 0 && !e.ids) return false;
+    return e.edges < (1ull << 31);
+}
+
+size_t edge_bytes(const cli_edges_t &e, size_t count) {
+    return e.offsets ? (count + 1) * sizeof(uint64_t) : 0;
+}
+
+EdgeSet to_set(const cli_edges_t &e) { return {e.offsets, e.ids, e.weights, e.offsets ? e.edges : 0}; }
+
+}  // namespace
+}  // namespace cli
+
+using namespace cli;
+
+extern "C" {
+
+const char *cli_status_name(int status) {
+    switch (status) {
+        case CLI_OK: return "ok";
+        case CLI_INVALID_ARGUMENT: return "invalid-argument";
+        case CLI_SHAPE_MISMATCH: return "shape-mismatch";
+        case CLI_UNSUPPORTED: return "unsupported";
+        case CLI_DEVICE: return "device";
+        case CLI_MALFORMED: return "malformed";
+        case CLI_INTERNAL: return "internal";
+        default: return "unknown";
+    }
+}
+
+// ----------------------------------------------------------------------------
+// pooled sigmoid pair loss
+// ----------------------------------------------------------------------------
+
+size_t pair_loss_sigmoid_workspace_bytes(size_t count, size_t width, size_t edges) {
+    return carve_pooled_workspace(nullptr, count, width, edges).bytes;
+}
+
+cli_status_t pair_loss_sigmoid_fwd_bwd(const cli_pair_loss_sigmoid_t *a) {
+    if (!a) return CLI_INVALID_ARGUMENT;
+    const cli_relations_t &rel = a->relations;
+    if (!a->embeddings || !a->inverse_temperature || !a->bias || !a->loss || !a->d_embeddings ||
+        !a->d_inverse_temperature || !a->d_bias || !a->device_status || !a->workspace)
+        return CLI_INVALID_ARGUMENT;
+    if (a->count < 2 || a->count >= (1ull << 31)) return CLI_SHAPE_MISMATCH;
+    if (a->width == 0 || a->width % 8 != 0 || a->ld < a->width || a->ld % 8 != 0) return CLI_SHAPE_MISMATCH;
+    if (a->width > 4096) return CLI_UNSUPPORTED;
+    if (a->ld_d_embeddings < a->width || a->ld_d_embeddings % 4 != 0) return CLI_SHAPE_MISMATCH;
+    if (!aligned(a->embeddings, 16) || !aligned(a->d_embeddings, 16) || !aligned(a->workspace, 256))
+        return CLI_INVALID_ARGUMENT;
+    if (!edges_ok(rel.attract) || !edges_ok(rel.repel) || !edges_ok(rel.ignore)) return CLI_INVALID_ARGUMENT;
+    // "a contrastive step naming no attract edge" is refused (Training, uform_trainer_step).
+    if (!rel.attract.offsets || rel.attract.edges == 0) return CLI_INVALID_ARGUMENT;
+    if (!(rel.ambient_weight >= 0.0f) || std::isinf(rel.ambient_weight)) return CLI_INVALID_ARGUMENT;
+    const size_t edges = rel.attract.edges + (rel.repel.offsets ? rel.repel.edges : 0) +
+                         (rel.ignore.offsets ? rel.ignore.edges : 0);
+    if (edges >= (1ull << 30)) return CLI_UNSUPPORTED;
+    const PooledWorkspace ws = carve_pooled_workspace(a->workspace, a->count, a->width, edges);
+    if (a->workspace_bytes < ws.bytes) return CLI_INVALID_ARGUMENT;
+
+    const size_t n = a->count;
+    const Range inputs[] = {
+        range_of(a->embeddings, ((n - 1) * a->ld + a->width) * 2),
+        range_of(a->inverse_temperature, 4),
+        range_of(a->bias, 4),
+        range_of(rel.attract.offsets, edge_bytes(rel.attract, n)),
+        range_of(rel.attract.ids, rel.attract.offsets ? rel.attract.edges * 4 : 0),
+        range_of(rel.attract.weights, rel.attract.offsets && rel.attract.weights ? rel.attract.edges * 4 : 0),
+        range_of(rel.repel.offsets, edge_bytes(rel.repel, n)),
+        range_of(rel.repel.ids, rel.repel.offsets ? rel.repel.edges * 4 : 0),
+        range_of(rel.repel.weights, rel.repel.offsets && rel.repel.weights ? rel.repel.edges * 4 : 0),
+        range_of(rel.ignore.offsets, edge_bytes(rel.ignore, n)),
+        range_of(rel.ignore.ids, rel.ignore.offsets ? rel.ignore.edges * 4 : 0),
+    };
+    const Range outputs[] = {
+        range_of(a->loss, 4),
+        range_of(a->d_embeddings, ((n - 1) * a->ld_d_embeddings + a->width) * 4),
+        range_of(a->d_inverse_temperature, 4),
+        range_of(a->d_bias, 4),
+        range_of(a->workspace, ws.bytes),
+        range_of(a->device_status, 4),
+    };
+    if (any_overlap(inputs, sizeof(inputs) / sizeof(inputs[0]), outputs, sizeof(outputs) / sizeof(outputs[0])))
+        return CLI_INVALID_ARGUMENT;
+
+    const int sms = sm_count();
+    if (sms <= 0) return CLI_DEVICE;
+    cudaStream_t stream = static_cast<cudaStream_t>(a->stream);
+    CUtensorMap tmap;
+    if (!encode_bf16_rows(&tmap, a->embeddings, a->width, n, a->ld)) return CLI_DEVICE;
+
+    if (cudaMemsetAsync(a->device_status, 0, sizeof(int32_t), stream) != cudaSuccess) return CLI_DEVICE;
+    const EdgeSet sets[3] = {to_set(rel.attract), to_set(rel.repel), to_set(rel.ignore)};
+    if (launch_relation_prep(sets, static_cast<int>(n), rel.negatives_named, rel.ambient_weight, ws, a->device_status,
+                             stream) != cudaSuccess)
+        return CLI_DEVICE;
+    if (cudaMemset2DAsync(a->d_embeddings, a->ld_d_embeddings * 4, 0, a->width * 4, n, stream) != cudaSuccess)
+        return CLI_DEVICE;
+    PooledLaunch L;
+    L.n = static_cast<int>(n);
+    L.width = static_cast<int>(a->width);
+    L.t_ptr = a->inverse_temperature;
+    L.b_ptr = a->bias;
+    L.ambient = rel.ambient_weight;
+    L.named = rel.negatives_named ? 1 : 0;
+    L.rel_off = ws.rel_off;
+    L.rel = ws.rel;
+    L.d_e = a->d_embeddings;
+    L.ld_de = static_cast<long long>(a->ld_d_embeddings);
+    L.partials = ws.partials;
+    L.loss = a->loss;
+    L.dt = a->d_inverse_temperature;
+    L.db = a->d_bias;
+    L.status = a->device_status;
+    L.sm_count = sms;
+    if (launch_pooled_fused(tmap, L, stream) != cudaSuccess) return CLI_DEVICE;
+    return CLI_OK;
+}
+
+// ----------------------------------------------------------------------------
+// sigmoid pair loss over a score matrix
+// ----------------------------------------------------------------------------
+
+size_t pair_loss_sigmoid_scores_workspace_bytes(size_t rows, size_t cols) {
+    return align256(static_cast<size_t>(score_loss_blocks(rows, cols)) * 4 * sizeof(float));
+}
+
+cli_status_t pair_loss_sigmoid_scores_fwd_bwd(const cli_pair_loss_sigmoid_scores_t *a) {
+    if (!a) return CLI_INVALID_ARGUMENT;
+    const cli_relations_t &rel = a->relations;
+    if (!a->scores || !a->inverse_temperature || !a->bias || !a->loss || !a->d_scores || !a->d_inverse_temperature ||
+        !a->d_bias || !a->device_status || !a->workspace)
+        return CLI_INVALID_ARGUMENT;
+    if (a->rows == 0 || a->cols == 0 || a->rows >= (1ull << 31) || a->cols >= (1ull << 31)) return CLI_SHAPE_MISMATCH;
+    if (a->ld < a->cols || a->ld_d_scores < a->cols) return CLI_SHAPE_MISMATCH;
+    if (a->sides && a->rows != a->cols) return CLI_SHAPE_MISMATCH;
+    if (!edges_ok(rel.attract) || !edges_ok(rel.repel) || !edges_ok(rel.ignore)) return CLI_INVALID_ARGUMENT;
+    if (!rel.attract.offsets || rel.attract.edges == 0) return CLI_INVALID_ARGUMENT;
+    if (!(rel.ambient_weight >= 0.0f) || std::isinf(rel.ambient_weight)) return CLI_INVALID_ARGUMENT;
+    if (a->workspace_bytes < pair_loss_sigmoid_scores_workspace_bytes(a->rows, a->cols)) return CLI_INVALID_ARGUMENT;
+    const size_t r = a->rows;
+    const Range inputs[] = {
+        range_of(a->scores, ((r - 1) * a->ld + a->cols) * 4),
+        range_of(a->inverse_temperature, 4),
+        range_of(a->bias, 4),
+        range_of(a->sides, a->sides ? r : 0),
+        range_of(rel.attract.offsets, edge_bytes(rel.attract, r)),
+        range_of(rel.attract.ids, rel.attract.offsets ? rel.attract.edges * 4 : 0),
+        range_of(rel.repel.offsets, edge_bytes(rel.repel, r)),
+        range_of(rel.repel.ids, rel.repel.offsets ? rel.repel.edges * 4 : 0),
+        range_of(rel.ignore.offsets, edge_bytes(rel.ignore, r)),
+        range_of(rel.ignore.ids, rel.ignore.offsets ? rel.ignore.edges * 4 : 0),
+    };
+    const Range outputs[] = {
+        range_of(a->loss, 4),
+        range_of(a->d_scores, ((r - 1) * a->ld_d_scores + a->cols) * 4),
+        range_of(a->d_inverse_temperature, 4),
+        range_of(a->d_bias, 4),
+        range_of(a->workspace, pair_loss_sigmoid_scores_workspace_bytes(a->rows, a->cols)),
+        range_of(a->device_status, 4),
+    };
+    if (any_overlap(inputs, sizeof(inputs) / sizeof(inputs[0]), outputs, sizeof(outputs) / sizeof(outputs[0])))
+        return CLI_INVALID_ARGUMENT;
+    cudaStream_t stream = static_cast<cudaStream_t>(a->stream);
+    if (cudaMemsetAsync(a->device_status, 0, sizeof(int32_t), stream) != cudaSuccess) return CLI_DEVICE;
+    ScoreLossLaunch L;
+    L.rows = static_cast<int>(a->rows);
+    L.cols = static_cast<int>(a->cols);
+    L.ld = static_cast<long long>(a->ld);
+    L.ld_ds = static_cast<long long>(a->ld_d_scores);
+    L.scores = a->scores;
+    L.t_ptr = a->inverse_temperature;
+    L.b_ptr = a->bias;
+    L.sets[0] = to_set(rel.attract);
+    L.sets[1] = to_set(rel.repel);
+    L.sets[2] = to_set(rel.ignore);
+    L.named = rel.negatives_named ? 1 : 0;
+    L.ambient = rel.ambient_weight;
+    L.sides = a->sides;
+    L.loss = a->loss;
+    L.d_scores = a->d_scores;
+    L.dt = a->d_inverse_temperature;
+    L.db = a->d_bias;
+    L.partials = static_cast<float *>(a->workspace);
+    L.blocks = score_loss_blocks(a->rows, a->cols);
+    L.status = a->device_status;
+    if (launch_score_loss(L, stream) != cudaSuccess) return CLI_DEVICE;
+    return CLI_OK;
+}
+
+// ----------------------------------------------------------------------------
+// MaxSim
+// ----------------------------------------------------------------------------
+
+namespace {
+
+bool tape_ok(const cli_tape_t &t) {
+    return t.data && t.offsets && t.count > 0 && t.rows >= t.count && t.rows < (1ull << 31) &&
+           t.count < (1ull << 31) && aligned(t.data, 16);
+}
+
+int chunk_rows_for(size_t rows_d, size_t rows_q, int sms) {
+    const long long mblocks = static_cast<long long>((rows_q + 127) / 128);
+    const long long target_items = 16LL * sms;
+    long long r = static_cast<long long>((static_cast<long double>(rows_d) * mblocks) / target_items);
+    if (r < 1024) r = 1024;
+    if (r > 16384) r = 16384;
+    return static_cast<int>((r + 127) / 128 * 128);
+}
+
+struct MaxSimWs {
+    float *mval;
+    uint32_t *chunk_doc;
+    size_t bytes;
+    int n_chunks, chunk_rows;
+};
+
+MaxSimWs carve_maxsim(void *base, size_t nd, size_t rows_q, size_t rows_d, int sms) {
+    MaxSimWs w;
+    uint8_t *p = static_cast<uint8_t *>(base);
+    size_t off = 0;
+    w.mval = reinterpret_cast<float *>(p ? p + off : nullptr);
+    off += align256(nd * rows_q * sizeof(float));
+    w.chunk_rows = chunk_rows_for(rows_d, rows_q, sms > 0 ? sms : 148);
+    w.n_chunks = static_cast<int>((rows_d + w.chunk_rows - 1) / w.chunk_rows);
+    w.chunk_doc = reinterpret_cast<uint32_t *>(p ? p + off : nullptr);
+    off += align256((static_cast<size_t>(w.n_chunks) + 1) * sizeof(uint32_t));
+    w.bytes = off;
+    return w;
+}
+
+}  // namespace
+
+size_t maxsim_workspace_bytes(size_t query_count, size_t document_count, size_t query_rows, size_t document_rows,
+                              size_t width) {
+    (void)query_count;
+    (void)width;
+    // The chunking depends on the SM count; size for the smallest chunks (most chunks).
+    const size_t chunks = (document_rows + 1023) / 1024 + 1;
+    return align256(document_count * query_rows * sizeof(float)) + align256((chunks + 1) * sizeof(uint32_t));
+}
+
+cli_status_t maxsim_scores(const cli_maxsim_t *a) {
+    if (!a) return CLI_INVALID_ARGUMENT;
+    if (!a->scores || !a->argmax || !a->device_status || !a->workspace) return CLI_INVALID_ARGUMENT;
+    if (!tape_ok(a->queries) || !tape_ok(a->documents)) return CLI_INVALID_ARGUMENT;
+    if (a->width == 0 || a->width % 8 != 0) return CLI_SHAPE_MISMATCH;
+    if (a->width > 256) return CLI_UNSUPPORTED;
+    const size_t nq = a->queries.count, nd = a->documents.count, rq = a->queries.rows, rd = a->documents.rows;
+    if (a->ld_scores < nd || a->ld_argmax < rq) return CLI_SHAPE_MISMATCH;
+    if (a->workspace_bytes < maxsim_workspace_bytes(nq, nd, rq, rd, a->width) || !aligned(a->workspace, 256))
+        return CLI_INVALID_ARGUMENT;
+    const Range inputs[] = {
+        range_of(a->queries.data, rq * a->width * 2), range_of(a->queries.offsets, (nq + 1) * 8),
+        range_of(a->documents.data, rd * a->width * 2), range_of(a->documents.offsets, (nd + 1) * 8),
+    };
+    const Range outputs[] = {
+        range_of(a->scores, ((nq - 1) * a->ld_scores + nd) * 4),
+        range_of(a->argmax, ((nd - 1) * a->ld_argmax + rq) * 4),
+        range_of(a->workspace, maxsim_workspace_bytes(nq, nd, rq, rd, a->width)),
+        range_of(a->device_status, 4),
+    };
+    if (any_overlap(inputs, 4, outputs, 4)) return CLI_INVALID_ARGUMENT;
+    const int sms = sm_count();
+    if (sms <= 0) return CLI_DEVICE;
+    const MaxSimWs ws = carve_maxsim(a->workspace, nd, rq, rd, sms);
+    cudaStream_t stream = static_cast<cudaStream_t>(a->stream);
+    CUtensorMap tq, td;
+    if (!encode_bf16_rows(&tq, a->queries.data, a->width, rq, a->width) ||
+        !encode_bf16_rows(&td, a->documents.data, a->width, rd, a->width))
+        return CLI_DEVICE;
+    if (cudaMemsetAsync(a->device_status, 0, sizeof(int32_t), stream) != cudaSuccess) return CLI_DEVICE;
+    if (launch_validate_tape(a->queries.offsets, static_cast<int>(nq), rq, a->device_status, stream) != cudaSuccess ||
+        launch_validate_tape(a->documents.offsets, static_cast<int>(nd), rd, a->device_status, stream) != cudaSuccess)
+        return CLI_DEVICE;
+    MaxSimLaunch L;
+    L.nq = static_cast<int>(nq);
+    L.nd = static_cast<int>(nd);
+    L.rows_q = static_cast<int>(rq);
+    L.rows_d = static_cast<int>(rd);
+    L.width = static_cast<int>(a->width);
+    L.mean = a->mean ? 1 : 0;
+    L.q_off = a->queries.offsets;
+    L.d_off = a->documents.offsets;
+    L.scores = a->scores;
+    L.ld_scores = static_cast<long long>(a->ld_scores);
+    L.argmax = a->argmax;
+    L.ld_argmax = static_cast<long long>(a->ld_argmax);
+    L.mval = ws.mval;
+    L.chunk_doc = ws.chunk_doc;
+    L.n_chunks = ws.n_chunks;
+    L.chunk_rows = ws.chunk_rows;
+    L.status = a->device_status;
+    L.sm_count = sms;
+    if (launch_maxsim_forward(tq, td, L, stream) != cudaSuccess) return CLI_DEVICE;
+    return CLI_OK;
+}
+
+size_t maxsim_backward_workspace_bytes(size_t query_count, size_t document_count, size_t query_rows,
+                                       size_t document_rows, size_t width) {
+    (void)query_count;
+    (void)document_count;
+    (void)document_rows;
+    (void)width;
+    return align256(query_rows * sizeof(int32_t));
+}
+
+cli_status_t maxsim_backward(const cli_maxsim_backward_t *a) {
+    if (!a) return CLI_INVALID_ARGUMENT;
+    if (!a->argmax || !a->d_scores || !a->d_queries || !a->d_documents || !a->device_status || !a->workspace)
+        return CLI_INVALID_ARGUMENT;
+    if (!tape_ok(a->queries) || !tape_ok(a->documents)) return CLI_INVALID_ARGUMENT;
+    if (a->width == 0 || a->width % 8 != 0) return CLI_SHAPE_MISMATCH;
+    if (a->width > 256) return CLI_UNSUPPORTED;
+    const size_t nq = a->queries.count, nd = a->documents.count, rq = a->queries.rows, rd = a->documents.rows;
+    if (a->ld_d_scores < nd || a->ld_argmax < rq) return CLI_SHAPE_MISMATCH;
+    if (!aligned(a->d_queries, 16) || !aligned(a->d_documents, 16)) return CLI_INVALID_ARGUMENT;
+    const size_t wsb = maxsim_backward_workspace_bytes(nq, nd, rq, rd, a->width);
+    if (a->workspace_bytes < wsb || !aligned(a->workspace, 256)) return CLI_INVALID_ARGUMENT;
+    const Range inputs[] = {
+        range_of(a->queries.data, rq * a->width * 2), range_of(a->queries.offsets, (nq + 1) * 8),
+        range_of(a->documents.data, rd * a->width * 2), range_of(a->documents.offsets, (nd + 1) * 8),
+        range_of(a->argmax, ((nd - 1) * a->ld_argmax + rq) * 4),
+        range_of(a->d_scores, ((nq - 1) * a->ld_d_scores + nd) * 4),
+    };
+    const Range outputs[] = {
+        range_of(a->d_queries, rq * a->width * 4),
+        range_of(a->d_documents, rd * a->width * 4),
+        range_of(a->workspace, wsb),
+        range_of(a->device_status, 4),
+    };
+    if (any_overlap(inputs, 6, outputs, 4)) return CLI_INVALID_ARGUMENT;
+    const int sms = sm_count();
+    if (sms <= 0) return CLI_DEVICE;
+    cudaStream_t stream = static_cast<cudaStream_t>(a->stream);
+    if (cudaMemsetAsync(a->device_status, 0, sizeof(int32_t), stream) != cudaSuccess) return CLI_DEVICE;
+    if (launch_validate_tape(a->queries.offsets, static_cast<int>(nq), rq, a->device_status, stream) != cudaSuccess ||
+        launch_validate_tape(a->documents.offsets, static_cast<int>(nd), rd, a->device_status, stream) != cudaSuccess)
+        return CLI_DEVICE;
+    MaxSimBwdLaunch L;
+    L.nq = static_cast<int>(nq);
+    L.nd = static_cast<int>(nd);
+    L.rows_q = static_cast<int>(rq);
+    L.rows_d = static_cast<int>(rd);
+    L.width = static_cast<int>(a->width);
+    L.mean = a->mean ? 1 : 0;
+    L.q_off = a->queries.offsets;
+    L.d_off = a->documents.offsets;
+    L.q = static_cast<const uint16_t *>(a->queries.data);
+    L.d = static_cast<const uint16_t *>(a->documents.data);
+    L.argmax = a->argmax;
+    L.ld_argmax = static_cast<long long>(a->ld_argmax);
+    L.d_scores = a->d_scores;
+    L.ld_ds = static_cast<long long>(a->ld_d_scores);
+    L.dq = a->d_queries;
+    L.dd = a->d_documents;
+    L.qmap = static_cast<int32_t *>(a->workspace);
+    L.status = a->device_status;
+    L.sm_count = sms;
+    if (launch_maxsim_backward(L, stream) != cudaSuccess) return CLI_DEVICE;
+    return CLI_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,126 @@
+// Internal interfaces between the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/cli.h"
+
+namespace cli {
+
+// One resolved "special" column of an anchor row: both directions of the pair
+// (row -> col and col -> row) with their weights (0 = skipped) and whether each
+// direction attracts (flags bit 0: row -> col, bit 1: col -> row).
+struct RelEntry {
+    uint32_t col;
+    float w_out;
+    float w_in;
+    uint32_t flags;
+};
+
+// Device view of one CSR edge set.
+struct EdgeSet {
+    const uint64_t *offsets;  // NULL = no edges
+    const uint32_t *ids;
+    const float *weights;     // NULL = weight one
+    uint64_t edges;
+};
+
+// Workspace carve-up for the pooled loss.
+struct PooledWorkspace {
+    uint32_t *indeg;       // [3][n]  in-degree counters, then fill cursors
+    uint32_t *tin_off;     // [3][n+1] transposed offsets
+    uint32_t *tin_ids;     // [E_total]  (set s at tin_base[s])
+    float *tin_w;          // [E_total]
+    uint32_t *rel_cnt;     // [n]
+    uint32_t *rel_off;     // [n+1]
+    RelEntry *rel;         // [2 E_total + n]
+    float *partials;       // [tile_pairs][4][4]
+    size_t bytes;
+};
+
+PooledWorkspace carve_pooled_workspace(void *base, size_t n, size_t width, size_t edges_total);
+size_t align256(size_t x);
+
+struct PooledLaunch {
+    int n, width;
+    const float *t_ptr, *b_ptr;
+    float ambient;
+    int named;
+    const uint32_t *rel_off;
+    const RelEntry *rel;
+    float *d_e;
+    long long ld_de;
+    float *partials;
+    float *loss, *dt, *db;
+    int32_t *status;
+    int sm_count;
+};
+
+// Relation preparation: validation, transposition and merged special lists.
+cudaError_t launch_relation_prep(const EdgeSet sets[3], int n, int named, float ambient, const PooledWorkspace &ws,
+                                 int32_t *status, cudaStream_t stream);
+
+cudaError_t launch_pooled_fused(const CUtensorMap &tmap_e, const PooledLaunch &L, cudaStream_t stream);
+size_t pooled_fused_smem_bytes();
+long long pooled_tile_pairs(int n);
+
+// Score-matrix loss.
+struct ScoreLossLaunch {
+    int rows, cols;
+    long long ld, ld_ds;
+    const float *scores;
+    const float *t_ptr, *b_ptr;
+    EdgeSet sets[3];
+    int named;
+    float ambient;
+    const uint8_t *sides;
+    float *loss, *d_scores, *dt, *db;
+    float *partials;       // [blocks][4]
+    int blocks;
+    int32_t *status;
+};
+cudaError_t launch_score_loss(const ScoreLossLaunch &L, cudaStream_t stream);
+int score_loss_blocks(size_t rows, size_t cols);
+
+// MaxSim.
+struct MaxSimLaunch {
+    int nq, nd, rows_q, rows_d, width, mean;
+    const uint64_t *q_off, *d_off;
+    float *scores;
+    long long ld_scores;
+    int32_t *argmax;
+    long long ld_argmax;
+    float *mval;              // workspace [nd][rows_q]
+    uint32_t *chunk_doc;      // workspace [n_chunks + 1]
+    int n_chunks, chunk_rows;
+    int32_t *status;
+    int sm_count;
+};
+cudaError_t launch_maxsim_forward(const CUtensorMap &tmap_q, const CUtensorMap &tmap_d, const MaxSimLaunch &L,
+                                  cudaStream_t stream);
+size_t maxsim_forward_smem_bytes(int width);
+
+struct MaxSimBwdLaunch {
+    int nq, nd, rows_q, rows_d, width, mean;
+    const uint64_t *q_off, *d_off;
+    const uint16_t *q, *d;
+    const int32_t *argmax;
+    long long ld_argmax;
+    const float *d_scores;
+    long long ld_ds;
+    float *dq, *dd;
+    int32_t *qmap;            // workspace [rows_q]
+    int32_t *status;
+    int sm_count;
+};
+cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream);
+
+// Shared validation kernels.
+cudaError_t launch_validate_edges(const EdgeSet &set, int n, int id_limit, int32_t *status, cudaStream_t stream);
+cudaError_t launch_validate_tape(const uint64_t *offsets, int count, uint64_t rows, int32_t *status,
+                                 cudaStream_t stream);
+
+}  // namespace cli

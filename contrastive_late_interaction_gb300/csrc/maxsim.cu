@@ -1,0 +1,477 @@
+// Hard MaxSim late interaction over ragged token tapes ("UForm", section
+// "ColBERT-Style Late-Interaction Rerankers"; tapes as in "Arenas", "Rows and
+// Tapes"):
+//     S(q, d) = sum_{t in q} max_{s in d} <q_t, d_s>   (optionally / |q|)
+// forward with the argmax, backward routed through it.
+//
+// GB300 design of the forward.  The whole query tape times the whole document
+// tape is one dense contraction with K = width, so it runs on tcgen05: a CTA
+// keeps a 128-row block of the query tape resident in shared memory and
+// streams 128-row tiles of the document tape through a TMA ring; each tile
+// product lands in one of two TMEM buffers.  Four epilogue warps read the
+// tiles back, one query row per thread, and keep a running (max, argmax) per
+// row across the tiles of the current document; the boundaries between
+// documents are the same for every row, so the segment logic is warp-uniform.
+// The max over a 32-column chunk is a tree of float max operations on keys that
+// carry the column in the 5 low mantissa bits (31 - column, so equal values
+// resolve to the lowest column), which costs about two instructions per cell;
+// the value it reports is truncated by less than 2^-18 relative.
+//
+// The ragged schedule: the document tape is cut into chunks of whole
+// documents of about `chunk_rows` rows (a binary search over the offsets per
+// chunk), and a work item is (chunk, query block).  Items run chunk-major, so
+// the CTAs running at the same time share one chunk of the document tape in L2.
+//
+// Per-row maxima go to a document-major workspace m[d][t]; a second kernel sums
+// them per query in a fixed order.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "cli_device.cuh"
+#include "cli_internal.h"
+
+namespace cli {
+namespace ms {
+
+constexpr int BM = 128;   // query rows per block
+constexpr int BN = 128;   // document rows per tile
+constexpr int BK = 64;    // K extent of one TMA box
+constexpr int STAGES = 2;
+constexpr uint32_t BOX_BYTES = 128 * BK * 2;   // 16 KB
+constexpr int kThreads = 192;
+constexpr uint32_t TMEM_COLS = 256;            // two 128-column score buffers
+
+struct Barriers {
+    uint64_t q_full, q_free, full[STAGES], empty[STAGES], s_full[2], s_free[2], mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// Dynamic shared memory: [Q: nk boxes][ring: STAGES x nk boxes][Barriers].
+__host__ __device__ inline size_t smem_bytes_for(int nk) {
+    return 1024 + static_cast<size_t>(nk) * BOX_BYTES * (1 + STAGES) + sizeof(Barriers);
+}
+
+struct Params {
+    int nq, nd, rows_q, rows_d, width, nk, mean;
+    int n_mblocks, n_chunks;
+    long long items;
+    const uint64_t *q_off, *d_off;
+    const uint32_t *chunk_doc;
+    int32_t *argmax;
+    long long ld_argmax;
+    float *mval;
+    int32_t *status;
+};
+
+// Running (max, argmax) update from 32 scores of one chunk, restricted to
+// columns [lo, hi) of the chunk.  c0 is the chunk's first tape row.
+template <bool kFull>
+__device__ __forceinline__ void chunk_max(const float (&v)[32], int lo, int hi, int c0, float &best, int &best_col) {
+    float key[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+        const float k = __int_as_float((__float_as_int(v[r]) & ~31) | (31 - r));
+        key[r] = kFull ? k : ((r >= lo && r < hi) ? k : -INFINITY);
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1)
+#pragma unroll
+        for (int r = 0; r < s; ++r) key[r] = fmaxf(key[r], key[r + s]);
+    const int bits = __float_as_int(key[0]);
+    const float val = __int_as_float(bits & ~31);
+    if (val > best) {
+        best = val;
+        best_col = c0 + (31 - (bits & 31));
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    forward_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_d, Params P) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *q_smem = base;
+    uint8_t *ring = base + static_cast<size_t>(P.nk) * BOX_BYTES;
+    Barriers &bar = *reinterpret_cast<Barriers *>(ring + static_cast<size_t>(STAGES) * P.nk * BOX_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (read_status(P.status) != 0) return;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bar.q_full, 1);
+        mbar_init(&bar.q_free, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&bar.full[s], 1);
+            mbar_init(&bar.empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar.s_full[s], 1);
+            mbar_init(&bar.s_free[s], 4);
+        }
+        mbar_init(&bar.mma_done, 1);
+        bar.abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmap_q);
+        prefetch_tmap(&tmap_d);
+    }
+    if (warp == 1) tmem_alloc(&bar.tmem_base, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bar.tmem_base;
+    volatile int *abort_flag = &bar.abort_flag;
+    const uint32_t stage_bytes = static_cast<uint32_t>(P.nk) * BOX_BYTES;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, it = 0;
+            bool ok = true;
+            for (long long w = blockIdx.x; w < P.items && ok; w += gridDim.x) {
+                const int chunk = static_cast<int>(w / P.n_mblocks), mb = static_cast<int>(w % P.n_mblocks);
+                const uint32_t d0 = P.chunk_doc[chunk], d1 = P.chunk_doc[chunk + 1];
+                if (d0 == d1) continue;
+                const long long r_lo = static_cast<long long>(P.d_off[d0]), r_hi = static_cast<long long>(P.d_off[d1]);
+                if (!mbar_wait(&bar.q_free, (it & 1) ^ 1, abort_flag, P.status)) break;
+                ++it;
+                mbar_arrive_expect_tx(&bar.q_full, stage_bytes);
+                for (int kc = 0; kc < P.nk; ++kc)
+                    tma_load_2d(q_smem + kc * BOX_BYTES, &tmap_q, &bar.q_full, kc * BK, mb * BM);
+                for (long long r0 = r_lo; r0 < r_hi; r0 += BN) {
+                    if (!mbar_wait(&bar.empty[stage], phase ^ 1, abort_flag, P.status)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&bar.full[stage], stage_bytes);
+                    uint8_t *dst = ring + static_cast<size_t>(stage) * stage_bytes;
+                    for (int kc = 0; kc < P.nk; ++kc)
+                        tma_load_2d(dst + kc * BOX_BYTES, &tmap_d, &bar.full[stage], kc * BK, static_cast<int>(r0));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            for (int s = 0; s < STAGES; ++s) {
+                mbar_wait(&bar.empty[stage], phase ^ 1, abort_flag, P.status);
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+            mbar_wait(&bar.q_free, (it & 1) ^ 1, abort_flag, P.status);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(128, 128, 0, 0);
+            const uint32_t qa = smem_u32(q_smem), ra = smem_u32(ring);
+            int stage = 0;
+            uint32_t phase = 0, it = 0, tc = 0;
+            bool ok = true;
+            for (long long w = blockIdx.x; w < P.items && ok; w += gridDim.x) {
+                const int chunk = static_cast<int>(w / P.n_mblocks);
+                const uint32_t d0 = P.chunk_doc[chunk], d1 = P.chunk_doc[chunk + 1];
+                if (d0 == d1) continue;
+                const long long r_lo = static_cast<long long>(P.d_off[d0]), r_hi = static_cast<long long>(P.d_off[d1]);
+                if (!mbar_wait(&bar.q_full, it & 1, abort_flag, P.status)) break;
+                ++it;
+                for (long long r0 = r_lo; r0 < r_hi; r0 += BN, ++tc) {
+                    const uint32_t buf = tc & 1;
+                    if (!mbar_wait(&bar.full[stage], phase, abort_flag, P.status)) { ok = false; break; }
+                    if (!mbar_wait(&bar.s_free[buf], ((tc >> 1) & 1) ^ 1, abort_flag, P.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t da = ra + stage * stage_bytes;
+                    for (int kc = 0; kc < P.nk; ++kc) {
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            const uint64_t a = sdesc_sw128(qa + kc * BOX_BYTES + kk * 32, 16, 1024);
+                            const uint64_t b = sdesc_sw128(da + kc * BOX_BYTES + kk * 32, 16, 1024);
+                            mma_bf16(tmem + buf * BN, a, b, idesc, (kc | kk) != 0);
+                        }
+                    }
+                    mma_commit(&bar.empty[stage]);
+                    mma_commit(&bar.s_full[buf]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                mma_commit(&bar.q_free);
+            }
+            mma_commit(&bar.mma_done);
+            mbar_wait(&bar.mma_done, 0, abort_flag, P.status);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue warps
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        uint32_t tc = 0;
+        bool ok = true;
+        for (long long w = blockIdx.x; w < P.items && ok; w += gridDim.x) {
+            const int chunk = static_cast<int>(w / P.n_mblocks), mb = static_cast<int>(w % P.n_mblocks);
+            const uint32_t d0 = P.chunk_doc[chunk], d1 = P.chunk_doc[chunk + 1];
+            if (d0 == d1) continue;
+            const long long r_lo = static_cast<long long>(P.d_off[d0]), r_hi = static_cast<long long>(P.d_off[d1]);
+            const int t = mb * BM + row;
+            const bool t_ok = t < P.rows_q;
+            uint32_t cur = d0;
+            long long cur_beg = r_lo, cur_end = static_cast<long long>(P.d_off[d0 + 1]);
+            float best = -INFINITY;
+            int best_col = 0;
+            for (long long r0 = r_lo; r0 < r_hi; r0 += BN, ++tc) {
+                const uint32_t buf = tc & 1;
+                if (!mbar_wait(&bar.s_full[buf], (tc >> 1) & 1, abort_flag, P.status)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll 1
+                for (int ch = 0; ch < BN / 32; ++ch) {
+                    const long long c0 = r0 + ch * 32;
+                    if (c0 >= r_hi) break;
+                    float v[32];
+                    tmem_ld32(tmem + lane_base + buf * BN + ch * 32, v);
+                    long long lo = c0;
+                    const long long hi_chunk = c0 + 32 < r_hi ? c0 + 32 : r_hi;
+                    while (lo < hi_chunk) {   // warp-uniform: document boundaries are shared by all rows
+                        const long long seg_hi = hi_chunk < cur_end ? hi_chunk : cur_end;
+                        const int a = static_cast<int>(lo - c0), b = static_cast<int>(seg_hi - c0);
+                        if (a == 0 && b == 32) chunk_max<true>(v, 0, 32, static_cast<int>(c0 - cur_beg), best, best_col);
+                        else chunk_max<false>(v, a, b, static_cast<int>(c0 - cur_beg), best, best_col);
+                        if (seg_hi == cur_end) {
+                            if (t_ok) {
+                                P.argmax[static_cast<long long>(cur) * P.ld_argmax + t] = best_col;
+                                P.mval[static_cast<long long>(cur) * P.rows_q + t] = best;
+                            }
+                            ++cur;
+                            best = -INFINITY;
+                            best_col = 0;
+                            if (cur < d1) {
+                                cur_beg = cur_end;
+                                cur_end = static_cast<long long>(P.d_off[cur + 1]);
+                            }
+                        }
+                        lo = seg_hi;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.s_free[buf]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// chunk_doc[k] = first document starting at or after row k * chunk_rows;
+// chunk_doc[n_chunks] = nd.
+__global__ void schedule_kernel(const uint64_t *d_off, int nd, int n_chunks, long long chunk_rows,
+                                uint32_t *chunk_doc, const int32_t *status) {
+    if (read_status(status) != 0) return;
+    const int k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (k > n_chunks) return;
+    if (k == n_chunks) {
+        chunk_doc[k] = static_cast<uint32_t>(nd);
+        return;
+    }
+    const uint64_t target = static_cast<uint64_t>(k) * static_cast<uint64_t>(chunk_rows);
+    int lo = 0, hi = nd;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (d_off[mid] < target) lo = mid + 1; else hi = mid;
+    }
+    chunk_doc[k] = static_cast<uint32_t>(lo);
+}
+
+// S[q][d] = sum over the query's rows of m[d][t], in row order (/ |q| if mean).
+__global__ void query_sum_kernel(const float *mval, const uint64_t *q_off, int nq, int nd, int rows_q, int mean,
+                                 float *scores, long long ld, const int32_t *status) {
+    if (read_status(status) != 0) return;
+    const long long total = static_cast<long long>(nq) * nd;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int d = static_cast<int>(idx / nq), q = static_cast<int>(idx % nq);
+        const uint64_t a = q_off[q], b = q_off[q + 1];
+        const float *m = mval + static_cast<long long>(d) * rows_q;
+        float s = 0.f;
+        for (uint64_t t = a; t < b; ++t) s += m[t];
+        if (mean) s /= static_cast<float>(b - a);
+        scores[static_cast<long long>(q) * ld + d] = s;
+    }
+}
+
+// ----------------------------------------------------------------------------
+// backward
+// ----------------------------------------------------------------------------
+
+__global__ void qmap_kernel(const uint64_t *q_off, int nq, int32_t *qmap, const int32_t *status) {
+    if (read_status(status) != 0) return;
+    const int q = blockIdx.x * blockDim.x + threadIdx.x;
+    if (q >= nq) return;
+    for (uint64_t t = q_off[q]; t < q_off[q + 1]; ++t) qmap[t] = q;
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&x)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// dQ[t] = sum_d c(q(t), d) * D[d_off[d] + argmax[d][t]]: 8 threads per query row,
+// each owning 8 features of every 64-feature block.  Gathers from the document
+// tape (L2 resident for the benchmark's sizes).
+constexpr int kDqRows = 32;
+__global__ void __launch_bounds__(256) dq_kernel(MaxSimBwdLaunch L) {
+    if (read_status(L.status) != 0) return;
+    const int t = blockIdx.x * kDqRows + (threadIdx.x >> 3);
+    const int sub = threadIdx.x & 7;
+    if (t >= L.rows_q) return;
+    const int q = L.qmap[t];
+    const float scale = L.mean ? 1.0f / static_cast<float>(L.q_off[q + 1] - L.q_off[q]) : 1.0f;
+    const int nblk = (L.width + 63) / 64;
+    float acc[4][8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[k][i] = 0.f;
+    const float *dsrow = L.d_scores + static_cast<long long>(q) * L.ld_ds;
+    for (int d = 0; d < L.nd; ++d) {
+        const int a = L.argmax[static_cast<long long>(d) * L.ld_argmax + t];
+        const uint64_t o0 = L.d_off[d], o1 = L.d_off[d + 1];
+        if (a < 0 || static_cast<uint64_t>(a) >= o1 - o0) {
+            report(L.status, CLI_MALFORMED);
+            continue;
+        }
+        const float c = dsrow[d] * scale;
+        const uint16_t *src = L.d + (o0 + static_cast<uint64_t>(a)) * L.width;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int f = k * 64 + sub * 8;
+            if (k < nblk && f < L.width) {
+                float x[8];
+                bf16x8_to_f32(__ldg(reinterpret_cast<const uint4 *>(src + f)), x);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[k][i] = fmaf(c, x[i], acc[k][i]);
+            }
+        }
+    }
+    float *dst = L.dq + static_cast<long long>(t) * L.width;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int f = k * 64 + sub * 8;
+        if (k < nblk && f < L.width) {
+            reinterpret_cast<float4 *>(dst + f)[0] = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+            reinterpret_cast<float4 *>(dst + f)[1] = make_float4(acc[k][4], acc[k][5], acc[k][6], acc[k][7]);
+        }
+    }
+}
+
+// dD rows of one document and one 32-feature slice, accumulated in shared
+// memory over every query row, in windows of kDdWindow document rows.
+constexpr int kDdWindow = 512;
+__global__ void __launch_bounds__(256) dd_kernel(MaxSimBwdLaunch L) {
+    __shared__ float acc[kDdWindow][32];
+    if (read_status(L.status) != 0) return;
+    const int d = blockIdx.x;
+    const int f = blockIdx.y * 32 + (threadIdx.x & 31);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t o0 = L.d_off[d];
+    const long long dl = static_cast<long long>(L.d_off[d + 1] - o0);
+    const int32_t *am = L.argmax + static_cast<long long>(d) * L.ld_argmax;
+    for (long long w0 = 0; w0 < dl; w0 += kDdWindow) {
+        const int wrows = static_cast<int>(dl - w0 < kDdWindow ? dl - w0 : kDdWindow);
+        for (int i = threadIdx.x; i < wrows * 32; i += blockDim.x) acc[i >> 5][i & 31] = 0.f;
+        __syncthreads();
+        for (int t0 = warp * 32; t0 < L.rows_q; t0 += 8 * 32) {
+            const int t = t0 + lane;
+            int a_l = -1;
+            float c_l = 0.f;
+            if (t < L.rows_q) {
+                a_l = am[t];
+                const int q = L.qmap[t];
+                const float scale = L.mean ? 1.0f / static_cast<float>(L.q_off[q + 1] - L.q_off[q]) : 1.0f;
+                c_l = L.d_scores[static_cast<long long>(q) * L.ld_ds + d] * scale;
+                if (a_l < 0 || a_l >= dl) {
+                    report(L.status, CLI_MALFORMED);
+                    a_l = -1;
+                }
+            }
+            const int jmax = min(32, L.rows_q - t0);
+            for (int j = 0; j < jmax; ++j) {
+                const int a = __shfl_sync(0xffffffffu, a_l, j);
+                const float c = __shfl_sync(0xffffffffu, c_l, j);
+                const long long ar = static_cast<long long>(a) - w0;
+                if (ar >= 0 && ar < wrows && f < L.width) {
+                    const float x = __uint_as_float(static_cast<uint32_t>(L.q[static_cast<long long>(t0 + j) * L.width + f]) << 16);
+                    atomicAdd(&acc[ar][lane], c * x);
+                }
+            }
+        }
+        __syncthreads();
+        if (f < L.width)
+            for (int r = warp; r < wrows; r += 8)
+                L.dd[(static_cast<long long>(o0) + w0 + r) * L.width + f] = acc[r][lane];
+        __syncthreads();
+    }
+}
+
+}  // namespace ms
+
+size_t maxsim_forward_smem_bytes(int width) { return ms::smem_bytes_for((width + ms::BK - 1) / ms::BK); }
+
+cudaError_t launch_maxsim_forward(const CUtensorMap &tmap_q, const CUtensorMap &tmap_d, const MaxSimLaunch &L,
+                                  cudaStream_t stream) {
+    using namespace ms;
+    cudaError_t err;
+    schedule_kernel<<<(L.n_chunks + 1 + 255) / 256, 256, 0, stream>>>(L.d_off, L.nd, L.n_chunks, L.chunk_rows,
+                                                                     L.chunk_doc, L.status);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    Params P;
+    P.nq = L.nq;
+    P.nd = L.nd;
+    P.rows_q = L.rows_q;
+    P.rows_d = L.rows_d;
+    P.width = L.width;
+    P.nk = (L.width + BK - 1) / BK;
+    P.mean = L.mean;
+    P.n_mblocks = (L.rows_q + BM - 1) / BM;
+    P.n_chunks = L.n_chunks;
+    P.items = static_cast<long long>(P.n_mblocks) * L.n_chunks;
+    P.q_off = L.q_off;
+    P.d_off = L.d_off;
+    P.chunk_doc = L.chunk_doc;
+    P.argmax = L.argmax;
+    P.ld_argmax = L.ld_argmax;
+    P.mval = L.mval;
+    P.status = L.status;
+    const size_t smem = smem_bytes_for(P.nk);
+    static size_t configured = 0;
+    if (configured < smem) {
+        if ((err = cudaFuncSetAttribute(forward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(smem))) != cudaSuccess)
+            return err;
+        configured = smem;
+    }
+    const int per_sm = smem * 2 + 2048 <= 233472 ? 2 : 1;
+    long long grid = static_cast<long long>(L.sm_count) * per_sm;
+    if (grid > P.items) grid = P.items;
+    forward_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmap_q, tmap_d, P);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    query_sum_kernel<<<L.sm_count * 8, 256, 0, stream>>>(L.mval, L.q_off, L.nq, L.nd, L.rows_q, L.mean, L.scores,
+                                                          L.ld_scores, L.status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream) {
+    using namespace ms;
+    cudaError_t err;
+    qmap_kernel<<<(L.nq + 255) / 256, 256, 0, stream>>>(L.q_off, L.nq, L.qmap, L.status);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    dq_kernel<<<(L.rows_q + kDqRows - 1) / kDqRows, 256, 0, stream>>>(L);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    dim3 grid(L.nd, (L.width + 31) / 32);
+    dd_kernel<<<grid, 256, 0, stream>>>(L);
+    return cudaGetLastError();
+}
+
+}  // namespace cli

@@ -1,0 +1,259 @@
+/*
+ * cli.h -- in-batch contrastive scoring on one GB300 (sm_103a): a stateless C ABI.
+ *
+ * Two operations of a multi-modal byte-encoder trainer's contrastive step, as
+ * the UForm 4 documentation pages describe them:
+ *
+ *   1. the pooled pair loss in SigLIP's `sigmoid` form over N pooled
+ *      embeddings, with a learnable inverse temperature t and bias b and
+ *      attract / repel / ignore relations given as CSR edge sets
+ *      ("UForm", section "Matryoshka-Like Multi-Scale Embedders", the SigLIP
+ *      loss; "Training", `uform_pair_loss_form_t`, `uform_contrastive_t`,
+ *      `uform_negatives_t`, `uform_edges_view_t`, `uform_relations_view_t`);
+ *   2. ColBERT-style hard MaxSim between query and document token vectors held
+ *      in Arrow-style ragged tapes, with a backward pass routed through the
+ *      argmax ("UForm", section "ColBERT-Style Late-Interaction Rerankers";
+ *      "Arenas", section "Rows and Tapes").
+ *
+ * Conventions, after the pages' C API ("Arenas"; "Training"):
+ *   - Callers lend memory and never a way to allocate it: every input, output
+ *     and workspace is a caller-owned device buffer, and the library allocates
+ *     nothing.  It enqueues work on the caller's stream and returns; it keeps
+ *     no pointer past return and holds no global state.
+ *   - Each verb takes one argument struct.
+ *   - Outputs are overwritten, never accumulated into.
+ *   - A fault the host can see (a NULL pointer, a bad size, an output
+ *     overlapping an input, a workspace that is too small, a misaligned
+ *     pointer) returns a status synchronously and enqueues nothing.
+ *   - A fault only the device can see (offsets that decrease or run past the
+ *     data, ids out of range or not strictly ascending, an empty query or
+ *     document, an argmax entry outside its document) is written to the
+ *     caller-lent `device_status` word (0 = success) by a validation kernel
+ *     that runs first on the stream; the compute kernels then do nothing and
+ *     the outputs are unspecified.  Nothing ever traps.  A device wait that
+ *     runs out of its bound reports CLI_INTERNAL there too.
+ *   - Status names are static strings (nothing allocates on failure).
+ *
+ * Element types: bf16 data are passed as `const void *` holding IEEE bfloat16
+ * values; every other element type is spelled out.  All pointers named
+ * "device" must be device memory of the current CUDA device; `stream` is a
+ * cudaStream_t (NULL = the legacy default stream).
+ */
+#ifndef CLI_H
+#define CLI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Statuses; the names follow the pages' status enumeration ("Python", section
+ * "Errors": shape-mismatch, unsupported, invalid-argument, device, malformed,
+ * internal). */
+typedef enum {
+    CLI_OK = 0,
+    CLI_INVALID_ARGUMENT = 1,
+    CLI_SHAPE_MISMATCH = 2,
+    CLI_UNSUPPORTED = 3,
+    CLI_DEVICE = 4,
+    CLI_MALFORMED = 5,
+    CLI_INTERNAL = 6
+} cli_status_t;
+
+/* Static name of a status ("ok", "invalid-argument", ...); "unknown" otherwise. */
+const char *cli_status_name(int status);
+
+/* One edge set over `count` items as compressed sparse rows ("Training",
+ * `uform_edges_view_t`): item i links to ids[offsets[i]] .. ids[offsets[i+1]-1],
+ * strictly ascending.  All three arrays are device memory; `offsets` NULL names
+ * no edges; `weights` NULL weighs every edge one.  `edges` must equal
+ * offsets[count] (checked on the device). */
+typedef struct {
+    const uint64_t *offsets; /* device, count + 1 */
+    const uint32_t *ids;     /* device, edges */
+    const float *weights;    /* device, edges, or NULL */
+    size_t edges;            /* host-side total, = offsets[count] */
+} cli_edges_t;
+
+/* Contrastive targets, resolved per ordered pair in this order ("Training",
+ * `uform_relations_view_t`): a pair `ignore` names is skipped, one `attract`
+ * names pulls (y = +1, its weight), one `repel` names pushes (y = -1, its
+ * weight), and every other pair follows the negatives: ambient
+ * (`negatives_named` = 0) repels at `ambient_weight`, named (1) skips it
+ * (`uform_negatives_t`).  Ignore weights are not read. */
+typedef struct {
+    cli_edges_t attract, repel, ignore;
+    int negatives_named;
+    float ambient_weight;
+} cli_relations_t;
+
+/*
+ * pair_loss_sigmoid_fwd_bwd -- the pooled sigmoid pair loss and its gradients.
+ *
+ * For every ordered pair (i, j), i != j, with resolved (y_ij, w_ij):
+ *     z_ij = t <e_i, e_j> + b,   l_ij = w_ij * (-log sigma(y_ij z_ij)),
+ *     L = (1/N) sum_{i != j} l_ij                        ("world mean"),
+ * and dL/dE (fp32), dL/dt, dL/db.  The N x N score matrix never reaches
+ * device memory: scores, sigmoids, log-sigmoids, relation masking and both
+ * gradient contractions are fused into one kernel over tiles.
+ *
+ *   count, width    N (> 1) and D (a multiple of 8, at most 4096)
+ *   embeddings      device bf16 [count x ld], row stride ld >= width (a
+ *                   multiple of 8), 16-byte aligned; the caller normalises
+ *   inverse_temperature, bias   device fp32 scalars t and b
+ *   relations       see cli_relations_t; a step naming no attract edge is
+ *                   refused with CLI_INVALID_ARGUMENT ("Training",
+ *                   `uform_trainer_step`, `relations`)
+ *   loss, d_inverse_temperature, d_bias   device fp32 scalars (written)
+ *   d_embeddings    device fp32 [count x ld_d_embeddings] (written), row
+ *                   stride a multiple of 4 and >= width, 16-byte aligned
+ *   workspace       device, >= pair_loss_sigmoid_workspace_bytes(...),
+ *                   256-byte aligned; contents on entry are ignored
+ *   device_status   device int32 (written: 0 or a cli_status_t)
+ *   stream          cudaStream_t
+ *
+ * dE sums tile contributions with reductions in whatever order the GPU runs
+ * them, so it is reproducible to rounding, not bit for bit; L, dt and db are
+ * reduced in a fixed order and are bit-reproducible.
+ */
+typedef struct {
+    size_t count, width, ld;
+    const void *embeddings;
+    const float *inverse_temperature;
+    const float *bias;
+    cli_relations_t relations;
+    float *loss;
+    float *d_embeddings;
+    size_t ld_d_embeddings;
+    float *d_inverse_temperature;
+    float *d_bias;
+    void *workspace;
+    size_t workspace_bytes;
+    int32_t *device_status;
+    void *stream;
+} cli_pair_loss_sigmoid_t;
+
+cli_status_t pair_loss_sigmoid_fwd_bwd(const cli_pair_loss_sigmoid_t *args);
+
+/* Workspace bytes for pair_loss_sigmoid_fwd_bwd; `edges` = the sum of the
+ * three edge sets' sizes. */
+size_t pair_loss_sigmoid_workspace_bytes(size_t count, size_t width, size_t edges);
+
+/*
+ * pair_loss_sigmoid_scores_fwd_bwd -- the same sigmoid pair loss over a given
+ * rows x cols score matrix S (e.g. hard MaxSim scores of queries against
+ * documents, "UForm", section "ColBERT-Style Late-Interaction Rerankers":
+ * the MaxSim scores fill the same band the embedder builds, and the SigLIP
+ * form stays selectable):
+ *     l_ij = w_ij * (-log sigma(y_ij (t S_ij + b))),  L = (1/rows) sum l_ij,
+ *     dS_ij = dL/dS_ij, dt, db.
+ * There is no implicit diagonal rule: rows and columns are different roles,
+ * and relations index rows -> columns.  With `sides` (rows == cols; one byte
+ * per item: bit 0 = can be a query, bit 1 = can be a document, after
+ * "Training", `uform_late_interaction_side_t`), every cell whose row item is
+ * not a query or whose column item is not a document is ignored.
+ *
+ *   scores          device fp32 [rows x ld]
+ *   d_scores        device fp32 [rows x ld_d_scores] (written)
+ *   other fields as in cli_pair_loss_sigmoid_t.
+ */
+typedef struct {
+    size_t rows, cols, ld;
+    const float *scores;
+    const float *inverse_temperature;
+    const float *bias;
+    cli_relations_t relations;
+    const uint8_t *sides; /* device, rows bytes, or NULL */
+    float *loss;
+    float *d_scores;
+    size_t ld_d_scores;
+    float *d_inverse_temperature;
+    float *d_bias;
+    void *workspace;
+    size_t workspace_bytes;
+    int32_t *device_status;
+    void *stream;
+} cli_pair_loss_sigmoid_scores_t;
+
+cli_status_t pair_loss_sigmoid_scores_fwd_bwd(const cli_pair_loss_sigmoid_scores_t *args);
+size_t pair_loss_sigmoid_scores_workspace_bytes(size_t rows, size_t cols);
+
+/* A ragged tape of `count` items ("Arenas", "Rows and Tapes"): item k owns rows
+ * offsets[k] .. offsets[k+1]-1 of `data`, which packs `rows` rows of `width`
+ * bf16 values end to end.  `data` and `offsets` are device memory; `rows`
+ * must equal offsets[count] (checked on the device); no item may be empty. */
+typedef struct {
+    const void *data;          /* device bf16 [rows x width], 16-byte aligned */
+    const uint64_t *offsets;   /* device, count + 1 */
+    size_t count, rows;
+} cli_tape_t;
+
+/*
+ * maxsim_scores -- hard MaxSim of every query against every document:
+ *     S(q, d) = sum_{t in q} max_{s in d} <q_t, d_s>       (mean = 0)
+ *     S(q, d) = (1/|q|) sum_{t in q} max_{s in d} <q_t, d_s>  (mean = 1)
+ * plus the argmax, the document-local index of the best row, lowest index on
+ * ties, for every query token and document.
+ *
+ *   width     token width D, a multiple of 8, at most 256 (the pages: a
+ *             multiple of 8, 128 by default)
+ *   scores    device fp32 [queries.count x ld_scores] (written)
+ *   argmax    device int32, document-major: argmax[d * ld_argmax + t] for
+ *             query-tape row t (ld_argmax >= queries.rows) (written)
+ *   workspace device, >= maxsim_workspace_bytes(...), 256-byte aligned
+ */
+typedef struct {
+    cli_tape_t queries, documents;
+    size_t width;
+    int mean;
+    float *scores;
+    size_t ld_scores;
+    int32_t *argmax;
+    size_t ld_argmax;
+    void *workspace;
+    size_t workspace_bytes;
+    int32_t *device_status;
+    void *stream;
+} cli_maxsim_t;
+
+cli_status_t maxsim_scores(const cli_maxsim_t *args);
+size_t maxsim_workspace_bytes(size_t query_count, size_t document_count, size_t query_rows,
+                              size_t document_rows, size_t width);
+
+/*
+ * maxsim_backward -- the gradient through the argmax: with
+ * c = dS[q][d] (divided by |q| when mean), for every query token t of q,
+ *     dQ[t]      += c * D[offsets_d + argmax[d][t]]
+ *     dD[offsets_d + argmax[d][t]] += c * Q[t].
+ *
+ *   argmax        device int32, the layout maxsim_scores writes
+ *   d_scores      device fp32 [queries.count x ld_d_scores]
+ *   d_queries     device fp32 [queries.rows x width] (written)
+ *   d_documents   device fp32 [documents.rows x width] (written)
+ */
+typedef struct {
+    cli_tape_t queries, documents;
+    size_t width;
+    int mean;
+    const int32_t *argmax;
+    size_t ld_argmax;
+    const float *d_scores;
+    size_t ld_d_scores;
+    float *d_queries;
+    float *d_documents;
+    void *workspace;
+    size_t workspace_bytes;
+    int32_t *device_status;
+    void *stream;
+} cli_maxsim_backward_t;
+
+cli_status_t maxsim_backward(const cli_maxsim_backward_t *args);
+size_t maxsim_backward_workspace_bytes(size_t query_count, size_t document_count, size_t query_rows,
+                                       size_t document_rows, size_t width);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CLI_H */

@@ -1,0 +1,90 @@
+"""Helpers shared by the GPU tests: uploading seeded inputs and comparing against the oracle."""
+
+import numpy as np
+import torch
+
+import contrastive_late_interaction_gb300 as cli
+
+# Tolerances (the acceptance bar): losses and scores 2e-3 relative, gradients 1e-2 relative L2,
+# argmax exact wherever the oracle's top-2 gap exceeds 1e-3.
+LOSS_RTOL = 2e-3
+SCORE_RTOL = 2e-3
+GRAD_RL2 = 1e-2
+ARGMAX_GAP = 1e-3
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).copy()).view(torch.bfloat16).to(dev())
+
+
+def i64(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.asarray(a, dtype=np.uint64).view(np.int64).copy()).to(dev())
+
+
+def scalar(x: float) -> torch.Tensor:
+    return torch.tensor([float(x)], dtype=torch.float32, device=dev())
+
+
+def rel_l2(a, b) -> float:
+    a, b = np.asarray(a, dtype=np.float64), np.asarray(b, dtype=np.float64)
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (den if den > 0 else 1.0))
+
+
+def assert_rel(a, b, rtol, what):
+    a, b = float(a), float(b)
+    assert abs(a - b) <= rtol * max(abs(b), 1e-30), f"{what}: gpu {a!r} oracle {b!r}"
+
+
+def run_pooled(p, weights=None, ld=None, ld_de=None, repel=None):
+    """Runs the pooled loss on the GPU for synth.PooledInputs p.  Returns numpy outputs and the status."""
+    e_bits = p.e_bf16
+    width = p.width
+    if ld is not None and ld > width:
+        e_bits = np.zeros((p.count, ld), dtype=np.uint16)
+        e_bits[:, :width] = p.e_bf16
+    e = bf16(e_bits)
+    out = {"width": width}
+    if ld_de is not None:
+        out["d_embeddings"] = torch.full((p.count, ld_de), 7.0, device=dev())[:, :width]
+    r = cli.pair_loss_sigmoid_fwd_bwd(e, scalar(p.t), scalar(p.b), cli.device_edges(p.attract),
+                                      cli.device_edges(repel if repel is not None else
+                                                       (p.repel if p.repel.ids.size else None)),
+                                      cli.device_edges(p.ignore if p.ignore.ids.size else None),
+                                      negatives_named=p.negatives_named, ambient_weight=p.ambient_weight, out=out)
+    torch.cuda.synchronize()
+    status = int(r["device_status"].item())
+    return dict(loss=r["loss"].item(), dt=r["d_inverse_temperature"].item(), db=r["d_bias"].item(),
+                de=r["d_embeddings"].double().cpu().numpy(), status=status, raw=r)
+
+
+def maxsim_tensors(m):
+    return bf16(m.q_bf16), i64(m.q_offsets), bf16(m.d_bf16), i64(m.d_offsets)
+
+
+def run_maxsim(m, mean=False, argmax=None):
+    q, qo, d, do = maxsim_tensors(m)
+    f = cli.maxsim_scores(q, qo, d, do, mean=mean)
+    am = f["argmax"] if argmax is None else torch.from_numpy(np.ascontiguousarray(argmax, dtype=np.int32)).to(dev())
+    ds = torch.from_numpy(np.ascontiguousarray(m.d_scores, dtype=np.float32)).to(dev())
+    g = cli.maxsim_backward(q, qo, d, do, am, ds, mean=mean)
+    torch.cuda.synchronize()
+    return dict(scores=f["scores"].double().cpu().numpy(), argmax=f["argmax"].cpu().numpy(),
+                dq=g["d_queries"].double().cpu().numpy(), dd=g["d_documents"].double().cpu().numpy(),
+                status_f=int(f["device_status"].item()), status_b=int(g["device_status"].item()))
+
+
+def check_scores(gpu, ref, what="scores"):
+    err = np.abs(gpu - ref) / np.maximum(np.abs(ref), 1.0)
+    assert err.max() <= SCORE_RTOL, f"{what}: max rel err {err.max():.3e}"
+
+
+def check_argmax(gpu, ref, gap):
+    sure = gap > ARGMAX_GAP
+    bad = np.count_nonzero(gpu[sure] != ref[sure])
+    assert bad == 0, f"{bad} argmax mismatches of {np.count_nonzero(sure)} decided entries"
+    return np.count_nonzero(sure)
