@@ -444,7 +444,9 @@ cudaError_t launch_maxsim_forward(const CUtensorMap &tmap_q, const CUtensorMap &
     P.ld_argmax = L.ld_argmax;
     P.mval = L.mval;
     P.status = L.status;
-    const size_t smem = smem_bytes_for(P.nk);
+    // At least 80 KB so that no more than two CTAs (2 x 256 TMEM columns) share an SM.
+    size_t smem = smem_bytes_for(P.nk);
+    if (smem < 80 * 1024) smem = 80 * 1024;
     static size_t configured = 0;
     if (configured < smem) {
         if ((err = cudaFuncSetAttribute(forward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
