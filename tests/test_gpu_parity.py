@@ -54,7 +54,7 @@ def test_pooled_ragged_weighted(n, width, named):
     """Ragged tiles (N and D not multiples of the tile), weighted attract and repel edges, ignores,
     both negatives modes, padded input and output row strides."""
     rng = np.random.default_rng(n + width)
-    p = synth.pooled_bags(3, n, width, ignore_p=0.02)
+    p = synth.pooled_bags(3, n, width, ignore_p=0.02, bag_size=2 if n == 2 else None)
     p.attract.weights = rng.uniform(0.2, 2.0, size=p.attract.ids.size).astype(np.float32)
     rep_lists = [sorted(set(rng.choice(n, size=min(n, 3), replace=False).tolist()) - {i}) for i in range(n)]
     rep = synth.edges_from_lists(rep_lists)
