@@ -121,7 +121,9 @@ EXPORTS = {
     "maxsim_workspace_bytes": (c_size_t, [c_size_t, c_size_t, c_size_t, c_size_t, c_size_t]),
     "maxsim_backward": (c_int, [ctypes.POINTER(MaxSimBackwardArgs)]),
     "maxsim_backward_workspace_bytes": (c_size_t, [c_size_t, c_size_t, c_size_t, c_size_t, c_size_t]),
+    "maxsim_backward_no_alloc": (c_int, [ctypes.POINTER(MaxSimBackwardArgs)]),
 }
+NO_ALLOC_MAX_QUERY_ROWS = 262144   # CLI_MAXSIM_NO_ALLOC_MAX_QUERY_ROWS in include/cli.h
 
 
 def _load():

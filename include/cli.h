@@ -19,7 +19,9 @@
  *   - Callers lend memory and never a way to allocate it: every input, output
  *     and workspace is a caller-owned device buffer, and the library allocates
  *     nothing.  It enqueues work on the caller's stream and returns; it keeps
- *     no pointer past return and holds no global state.
+ *     no pointer past return and holds no global state (one entry point,
+ *     maxsim_backward_no_alloc, keeps a fixed scratch array instead of a
+ *     lent workspace; see there).
  *   - Each verb takes one argument struct.
  *   - Outputs are overwritten, never accumulated into.
  *   - A fault the host can see (a NULL pointer, a bad size, an output
@@ -252,6 +254,27 @@ typedef struct {
 cli_status_t maxsim_backward(const cli_maxsim_backward_t *args);
 size_t maxsim_backward_workspace_bytes(size_t query_count, size_t document_count, size_t query_rows,
                                        size_t document_rows, size_t width);
+
+/*
+ * maxsim_backward_no_alloc -- maxsim_backward for callers that cannot allocate
+ * device memory and have no buffer to lend as workspace: code running where an
+ * allocation is not allowed or would stall the device, or a runtime whose
+ * device memory is all reserved by its own allocator.  The pages have no
+ * counterpart; this entry point exists only for such callers.
+ *
+ * Same arguments and results as maxsim_backward; `workspace` and
+ * `workspace_bytes` are not read.  Its one piece of scratch (the query of every
+ * query-tape row) lives in a fixed device array of
+ * CLI_MAXSIM_NO_ALLOC_MAX_QUERY_ROWS int32 entries (1 MiB) that every GPU
+ * loading the library holds until the process exits.  A query tape of more
+ * rows returns CLI_UNSUPPORTED.  Every call shares that array: calls whose
+ * kernels overlap on the GPU (other streams or host threads) race on it.  The
+ * first call on each device looks the array's address up and caches it; make
+ * that call before any stream capture.  Nothing here calls cudaMalloc, cudaFree
+ * or any allocating routine.
+ */
+#define CLI_MAXSIM_NO_ALLOC_MAX_QUERY_ROWS 262144
+cli_status_t maxsim_backward_no_alloc(const cli_maxsim_backward_t *args);
 
 #ifdef __cplusplus
 }
