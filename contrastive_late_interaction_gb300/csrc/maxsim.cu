@@ -67,24 +67,31 @@ struct Params {
 };
 
 // Running (max, argmax) update from 32 scores of one chunk, restricted to
-// columns [lo, hi) of the chunk.  c0 is the chunk's first tape row.
+// columns [lo, hi) of the chunk; `base` is the chunk's first row relative to
+// the current document.  Keys carry 31 - column in the 5 low mantissa bits, so
+// the max of the keys names the lowest column among equal values; the tree
+// uses the three-input max (16 instructions for 32 keys).
 template <bool kFull>
-__device__ __forceinline__ void chunk_max(const float (&v)[32], int lo, int hi, int c0, float &best, int &best_col) {
+__device__ __forceinline__ void chunk_max(const float (&v)[32], int lo, int hi, int base, float &best, int &best_col) {
     float key[32];
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
         const float k = __int_as_float((__float_as_int(v[r]) & ~31) | (31 - r));
         key[r] = kFull ? k : ((r >= lo && r < hi) ? k : -INFINITY);
     }
+    float m[12];
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1)
-#pragma unroll
-        for (int r = 0; r < s; ++r) key[r] = fmaxf(key[r], key[r + s]);
-    const int bits = __float_as_int(key[0]);
+    for (int i = 0; i < 10; ++i) m[i] = fmax3(key[3 * i], key[3 * i + 1], key[3 * i + 2]);
+    m[10] = key[30];
+    m[11] = key[31];
+    const float n0 = fmax3(m[0], m[1], m[2]), n1 = fmax3(m[3], m[4], m[5]);
+    const float n2 = fmax3(m[6], m[7], m[8]), n3 = fmax3(m[9], m[10], m[11]);
+    const float top = fmaxf(fmax3(n0, n1, n2), n3);
+    const int bits = __float_as_int(top);
     const float val = __int_as_float(bits & ~31);
     if (val > best) {
         best = val;
-        best_col = c0 + (31 - (bits & 31));
+        best_col = base + (31 - (bits & 31));
     }
 }
 
@@ -205,30 +212,48 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int chunk = static_cast<int>(w / P.n_mblocks), mb = static_cast<int>(w % P.n_mblocks);
             const uint32_t d0 = P.chunk_doc[chunk], d1 = P.chunk_doc[chunk + 1];
             if (d0 == d1) continue;
-            const long long r_lo = static_cast<long long>(P.d_off[d0]), r_hi = static_cast<long long>(P.d_off[d1]);
+            // Positions below are 32-bit offsets from the item's first row.
+            const long long r_lo = static_cast<long long>(P.d_off[d0]);
+            const int span = static_cast<int>(static_cast<long long>(P.d_off[d1]) - r_lo);
             const int t = mb * BM + row;
             const bool t_ok = t < P.rows_q;
             uint32_t cur = d0;
-            long long cur_beg = r_lo, cur_end = static_cast<long long>(P.d_off[d0 + 1]);
+            int cur_beg = 0, cur_end = static_cast<int>(static_cast<long long>(P.d_off[d0 + 1]) - r_lo);
             float best = -INFINITY;
             int best_col = 0;
-            for (long long r0 = r_lo; r0 < r_hi; r0 += BN, ++tc) {
+            for (int r0 = 0; r0 < span; r0 += BN, ++tc) {
                 const uint32_t buf = tc & 1;
                 if (!mbar_wait(&bar.s_full[buf], (tc >> 1) & 1, abort_flag, P.status)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll 1
                 for (int ch = 0; ch < BN / 32; ++ch) {
-                    const long long c0 = r0 + ch * 32;
-                    if (c0 >= r_hi) break;
+                    const int c0 = r0 + ch * 32;
+                    if (c0 >= span) break;
                     float v[32];
                     tmem_ld32(tmem + lane_base + buf * BN + ch * 32, v);
-                    long long lo = c0;
-                    const long long hi_chunk = c0 + 32 < r_hi ? c0 + 32 : r_hi;
+                    const int hi_chunk = min(c0 + 32, span);
+                    if (hi_chunk == c0 + 32 && cur_end >= c0 + 32) {
+                        // the whole chunk lies inside the current document
+                        chunk_max<true>(v, 0, 32, c0 - cur_beg, best, best_col);
+                        if (cur_end == c0 + 32) {
+                            if (t_ok) {
+                                P.argmax[static_cast<long long>(cur) * P.ld_argmax + t] = best_col;
+                                P.mval[static_cast<long long>(cur) * P.rows_q + t] = best;
+                            }
+                            ++cur;
+                            best = -INFINITY;
+                            best_col = 0;
+                            if (cur < d1) {
+                                cur_beg = cur_end;
+                                cur_end = static_cast<int>(static_cast<long long>(P.d_off[cur + 1]) - r_lo);
+                            }
+                        }
+                        continue;
+                    }
+                    int lo = c0;
                     while (lo < hi_chunk) {   // warp-uniform: document boundaries are shared by all rows
-                        const long long seg_hi = hi_chunk < cur_end ? hi_chunk : cur_end;
-                        const int a = static_cast<int>(lo - c0), b = static_cast<int>(seg_hi - c0);
-                        if (a == 0 && b == 32) chunk_max<true>(v, 0, 32, static_cast<int>(c0 - cur_beg), best, best_col);
-                        else chunk_max<false>(v, a, b, static_cast<int>(c0 - cur_beg), best, best_col);
+                        const int seg_hi = min(hi_chunk, cur_end);
+                        chunk_max<false>(v, lo - c0, seg_hi - c0, c0 - cur_beg, best, best_col);
                         if (seg_hi == cur_end) {
                             if (t_ok) {
                                 P.argmax[static_cast<long long>(cur) * P.ld_argmax + t] = best_col;
@@ -239,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                             best_col = 0;
                             if (cur < d1) {
                                 cur_beg = cur_end;
-                                cur_end = static_cast<long long>(P.d_off[cur + 1]);
+                                cur_end = static_cast<int>(static_cast<long long>(P.d_off[cur + 1]) - r_lo);
                             }
                         }
                         lo = seg_hi;
@@ -317,10 +342,14 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&x)[8]) {
     }
 }
 
-// dQ[t] = sum_d c(q(t), d) * D[d_off[d] + argmax[d][t]]: 8 threads per query row,
-// each owning 8 features of every 64-feature block.  Gathers from the document
-// tape (L2 resident for the benchmark's sizes).
+// dQ[t] = sum_d c(q(t), d) * D[d_off[d] + argmax[d][t]]: 8 threads per query
+// row, each owning 8 features of every 64-feature block.  Documents go in
+// groups of 8 whose argmax entries, upstream gradients and offsets are loaded
+// before any of the 8 row gathers is used, so every thread keeps 8 x 16-byte
+// gathers (per feature block) in flight.
 constexpr int kDqRows = 32;
+constexpr int kDqUnroll = 8;
+template <int NBLK>   // 64-feature blocks of the width (1..4)
 __global__ void __launch_bounds__(256) dq_kernel(MaxSimBwdLaunch L) {
     if (read_status(L.status) != 0) return;
     const int t = blockIdx.x * kDqRows + (threadIdx.x >> 3);
@@ -328,89 +357,139 @@ __global__ void __launch_bounds__(256) dq_kernel(MaxSimBwdLaunch L) {
     if (t >= L.rows_q) return;
     const int q = L.qmap[t];
     const float scale = L.mean ? 1.0f / static_cast<float>(L.q_off[q + 1] - L.q_off[q]) : 1.0f;
-    const int nblk = (L.width + 63) / 64;
-    float acc[4][8];
+    constexpr int nblk = NBLK;
+    float acc[NBLK][8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+    for (int k = 0; k < NBLK; ++k)
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[k][i] = 0.f;
     const float *dsrow = L.d_scores + static_cast<long long>(q) * L.ld_ds;
-    for (int d = 0; d < L.nd; ++d) {
-        const int a = L.argmax[static_cast<long long>(d) * L.ld_argmax + t];
-        const uint64_t o0 = L.d_off[d], o1 = L.d_off[d + 1];
-        if (a < 0 || static_cast<uint64_t>(a) >= o1 - o0) {
-            report(L.status, CLI_MALFORMED);
-            continue;
+    const int32_t *amcol = L.argmax + t;
+    for (int d0 = 0; d0 < L.nd; d0 += kDqUnroll) {
+        int a[kDqUnroll];
+        float c[kDqUnroll];
+        uint64_t o[kDqUnroll + 1];
+#pragma unroll
+        for (int u = 0; u < kDqUnroll; ++u) {
+            const int d = d0 + u;
+            a[u] = d < L.nd ? __ldg(amcol + static_cast<long long>(d) * L.ld_argmax) : 0;
+            c[u] = d < L.nd ? __ldg(dsrow + d) * scale : 0.f;
         }
-        const float c = dsrow[d] * scale;
-        const uint16_t *src = L.d + (o0 + static_cast<uint64_t>(a)) * L.width;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int f = k * 64 + sub * 8;
-            if (k < nblk && f < L.width) {
-                float x[8];
-                bf16x8_to_f32(__ldg(reinterpret_cast<const uint4 *>(src + f)), x);
+        for (int u = 0; u <= kDqUnroll; ++u) o[u] = __ldg(L.d_off + min(d0 + u, L.nd));
+        uint4 x[kDqUnroll][NBLK];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[k][i] = fmaf(c, x[i], acc[k][i]);
+        for (int u = 0; u < kDqUnroll; ++u) {
+            const uint64_t len = o[u + 1] - o[u];
+            const bool valid = d0 + u < L.nd;
+            if (valid && (a[u] < 0 || static_cast<uint64_t>(a[u]) >= len)) {
+                report(L.status, CLI_MALFORMED);
+                c[u] = 0.f;
+                a[u] = 0;
+            }
+            const uint16_t *src = L.d + (o[u] + static_cast<uint64_t>(valid ? a[u] : 0)) * L.width;
+#pragma unroll
+            for (int k = 0; k < NBLK; ++k) {
+                const int f = k * 64 + sub * 8;
+                x[u][k] = (valid && f < L.width) ? __ldg(reinterpret_cast<const uint4 *>(src + f))
+                                                 : make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kDqUnroll; ++u) {
+#pragma unroll
+            for (int k = 0; k < NBLK; ++k) {
+                float v[8];
+                bf16x8_to_f32(x[u][k], v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[k][i] = fmaf(c[u], v[i], acc[k][i]);
             }
         }
     }
+    (void)nblk;
     float *dst = L.dq + static_cast<long long>(t) * L.width;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < NBLK; ++k) {
         const int f = k * 64 + sub * 8;
-        if (k < nblk && f < L.width) {
+        if (f < L.width) {
             reinterpret_cast<float4 *>(dst + f)[0] = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
             reinterpret_cast<float4 *>(dst + f)[1] = make_float4(acc[k][4], acc[k][5], acc[k][6], acc[k][7]);
         }
     }
 }
 
-// dD rows of one document and one 32-feature slice, accumulated in shared
-// memory over every query row, in windows of kDdWindow document rows.
+// dD rows of one document and one 64-feature slice: a window of up to
+// kDdWindow document rows accumulates in shared memory (fp32).  Each warp takes
+// 32 query rows at a time: lane j loads row j's argmax entry and c(q, d), then
+// the warp walks the 32 rows with lanes as features (lane l adds features l and
+// l + 32 of the row), so the loads of a query row are coalesced and the shared
+// adds of one instruction hit 32 consecutive words.  The window test is
+// warp-uniform.
 constexpr int kDdWindow = 512;
-__global__ void __launch_bounds__(256) dd_kernel(MaxSimBwdLaunch L) {
-    __shared__ float acc[kDdWindow][32];
+constexpr int kDdThreads = 512;
+constexpr int kDdUnroll = 8;
+__global__ void __launch_bounds__(kDdThreads, 1) dd_kernel(MaxSimBwdLaunch L) {
+    extern __shared__ float dd_acc[];      // [kDdWindow][64]
     if (read_status(L.status) != 0) return;
     const int d = blockIdx.x;
-    const int f = blockIdx.y * 32 + (threadIdx.x & 31);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int f0 = blockIdx.y * 64;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int kWarps = kDdThreads / 32;
     const uint64_t o0 = L.d_off[d];
     const long long dl = static_cast<long long>(L.d_off[d + 1] - o0);
     const int32_t *am = L.argmax + static_cast<long long>(d) * L.ld_argmax;
+    const bool f_lo = f0 + lane < L.width, f_hi = f0 + 32 + lane < L.width;
     for (long long w0 = 0; w0 < dl; w0 += kDdWindow) {
         const int wrows = static_cast<int>(dl - w0 < kDdWindow ? dl - w0 : kDdWindow);
-        for (int i = threadIdx.x; i < wrows * 32; i += blockDim.x) acc[i >> 5][i & 31] = 0.f;
+        for (int i = threadIdx.x; i < wrows * 64; i += kDdThreads) dd_acc[i] = 0.f;
         __syncthreads();
-        for (int t0 = warp * 32; t0 < L.rows_q; t0 += 8 * 32) {
+        for (int t0 = warp * 32; t0 < L.rows_q; t0 += kWarps * 32) {
             const int t = t0 + lane;
             int a_l = -1;
             float c_l = 0.f;
             if (t < L.rows_q) {
-                a_l = am[t];
-                const int q = L.qmap[t];
-                const float scale = L.mean ? 1.0f / static_cast<float>(L.q_off[q + 1] - L.q_off[q]) : 1.0f;
-                c_l = L.d_scores[static_cast<long long>(q) * L.ld_ds + d] * scale;
+                a_l = __ldg(am + t);
                 if (a_l < 0 || a_l >= dl) {
                     report(L.status, CLI_MALFORMED);
                     a_l = -1;
+                } else {
+                    const int q = __ldg(L.qmap + t);
+                    c_l = __ldg(L.d_scores + static_cast<long long>(q) * L.ld_ds + d);
+                    if (L.mean) c_l /= static_cast<float>(L.q_off[q + 1] - L.q_off[q]);
                 }
+                const long long ar = static_cast<long long>(a_l) - w0;
+                if (a_l >= 0 && (ar < 0 || ar >= wrows)) a_l = -1;    // outside this window
             }
             const int jmax = min(32, L.rows_q - t0);
-            for (int j = 0; j < jmax; ++j) {
-                const int a = __shfl_sync(0xffffffffu, a_l, j);
-                const float c = __shfl_sync(0xffffffffu, c_l, j);
-                const long long ar = static_cast<long long>(a) - w0;
-                if (ar >= 0 && ar < wrows && f < L.width) {
-                    const float x = __uint_as_float(static_cast<uint32_t>(L.q[static_cast<long long>(t0 + j) * L.width + f]) << 16);
-                    atomicAdd(&acc[ar][lane], c * x);
+            for (int j0 = 0; j0 < jmax; j0 += kDdUnroll) {
+                uint16_t x0[kDdUnroll], x1[kDdUnroll];
+                int a[kDdUnroll];
+                float c[kDdUnroll];
+#pragma unroll
+                for (int u = 0; u < kDdUnroll; ++u) {
+                    const int j = j0 + u;
+                    a[u] = __shfl_sync(0xffffffffu, a_l, j & 31);
+                    c[u] = __shfl_sync(0xffffffffu, c_l, j & 31);
+                    if (j >= jmax) a[u] = -1;
+                    const uint16_t *src = L.q + static_cast<long long>(t0 + j) * L.width + f0;
+                    x0[u] = (a[u] >= 0 && f_lo) ? __ldg(src + lane) : 0;
+                    x1[u] = (a[u] >= 0 && f_hi) ? __ldg(src + 32 + lane) : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < kDdUnroll; ++u) {
+                    if (a[u] >= 0) {
+                        float *row = dd_acc + (static_cast<long long>(a[u]) - w0) * 64;
+                        atomicAdd(row + lane, c[u] * __uint_as_float(static_cast<uint32_t>(x0[u]) << 16));
+                        atomicAdd(row + 32 + lane, c[u] * __uint_as_float(static_cast<uint32_t>(x1[u]) << 16));
+                    }
                 }
             }
         }
         __syncthreads();
-        if (f < L.width)
-            for (int r = warp; r < wrows; r += 8)
-                L.dd[(static_cast<long long>(o0) + w0 + r) * L.width + f] = acc[r][lane];
+        for (int i = threadIdx.x; i < wrows * 64; i += kDdThreads) {
+            const int r = i >> 6, f = i & 63;
+            if (f0 + f < L.width) L.dd[(static_cast<long long>(o0) + w0 + r) * L.width + f0 + f] = dd_acc[i];
+        }
         __syncthreads();
     }
 }
@@ -469,10 +548,20 @@ cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream
     cudaError_t err;
     qmap_kernel<<<(L.nq + 255) / 256, 256, 0, stream>>>(L.q_off, L.nq, L.qmap, L.status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    dq_kernel<<<(L.rows_q + kDqRows - 1) / kDqRows, 256, 0, stream>>>(L);
+    const unsigned dq_grid = (L.rows_q + kDqRows - 1) / kDqRows;
+    switch ((L.width + 63) / 64) {
+        case 1: dq_kernel<1><<<dq_grid, 256, 0, stream>>>(L); break;
+        case 2: dq_kernel<2><<<dq_grid, 256, 0, stream>>>(L); break;
+        case 3: dq_kernel<3><<<dq_grid, 256, 0, stream>>>(L); break;
+        default: dq_kernel<4><<<dq_grid, 256, 0, stream>>>(L); break;
+    }
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    dim3 grid(L.nd, (L.width + 31) / 32);
-    dd_kernel<<<grid, 256, 0, stream>>>(L);
+    const size_t dd_smem = static_cast<size_t>(kDdWindow) * 64 * sizeof(float);
+    if ((err = cudaFuncSetAttribute(dd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(dd_smem))) != cudaSuccess)
+        return err;
+    dim3 grid(L.nd, (L.width + 63) / 64);
+    dd_kernel<<<grid, kDdThreads, dd_smem, stream>>>(L);
     return cudaGetLastError();
 }
 

@@ -95,20 +95,33 @@ __global__ void __launch_bounds__(kThreads) score_loss_kernel(ScoreLossLaunch L)
     }
 }
 
+// Sums the per-block partials in a fixed order: thread k adds blocks k, k+256,
+// ... in order, then a fixed-shape tree over the 256 threads.
 __global__ void score_finish_kernel(const float *partials, int blocks, int rows, float *loss, float *dt, float *db,
                                     const int32_t *status) {
     if (read_status(status) != 0) return;
-    if (threadIdx.x != 0) return;
+    __shared__ double red[3][256];
     double l = 0, gs = 0, g = 0;
-    for (int k = 0; k < blocks; ++k) {
+    for (int k = threadIdx.x; k < blocks; k += blockDim.x) {
         l += partials[k * 4 + 0];
         gs += partials[k * 4 + 1];
         g += partials[k * 4 + 2];
     }
-    const double inv = 1.0 / static_cast<double>(rows);
-    *loss = static_cast<float>(l * inv);
-    *dt = static_cast<float>(gs * inv);
-    *db = static_cast<float>(g * inv);
+    red[0][threadIdx.x] = l;
+    red[1][threadIdx.x] = gs;
+    red[2][threadIdx.x] = g;
+    __syncthreads();
+    for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w)
+            for (int c = 0; c < 3; ++c) red[c][threadIdx.x] += red[c][threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const double inv = 1.0 / static_cast<double>(rows);
+        *loss = static_cast<float>(red[0][0] * inv);
+        *dt = static_cast<float>(red[1][0] * inv);
+        *db = static_cast<float>(red[2][0] * inv);
+    }
 }
 
 }  // namespace
@@ -127,7 +140,7 @@ cudaError_t launch_score_loss(const ScoreLossLaunch &L, cudaStream_t stream) {
         if ((err = launch_validate_edges(L.sets[s], L.rows, L.cols, L.status, stream)) != cudaSuccess) return err;
     score_loss_kernel<<<L.blocks, kThreads, 0, stream>>>(L);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    score_finish_kernel<<<1, 32, 0, stream>>>(L.partials, L.blocks, L.rows, L.loss, L.dt, L.db, L.status);
+    score_finish_kernel<<<1, 256, 0, stream>>>(L.partials, L.blocks, L.rows, L.loss, L.dt, L.db, L.status);
     return cudaGetLastError();
 }
 
