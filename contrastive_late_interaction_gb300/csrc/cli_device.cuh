@@ -51,9 +51,24 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
-// One bounded probe of the barrier: the thread may be suspended (up to the
-// hint, 0.5 ms) until the phase completes, instead of spinning on issue slots.
+// One probe of the barrier (the hardware may briefly suspend the thread).
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// A probe that lets the thread sleep up to `hint_ns` while the phase is open,
+// for waits that have already lasted a while.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t ok;
     asm volatile(
         "{\n"
@@ -62,7 +77,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         " selp.u32 %0, 1, 0, p;\n"
         "}\n"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(500000u)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
@@ -78,13 +93,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // waiter of the CTA sees the flag and gives up too, so the kernel returns.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+// `sleep_ns` > 0 puts the thread to sleep that long between failed probes, so a
+// waiter whose wake-up is not on the critical path (a TMA producer, say) leaves
+// the issue slots to the warps doing the work.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *status) {
+                                          int32_t *status, uint32_t sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t spin = 1;; ++spin) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((spin & 15u) == 0) {
+        if (sleep_ns) __nanosleep(sleep_ns);
+        // short waits probe without sleeping; long ones sleep in 20 us steps
+        if (spin < 4096 ? mbar_try_wait(bar, parity) : mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if ((spin & 255u) == 0) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
                 *abort_flag = 1;
@@ -94,6 +114,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
         }
     }
 }
+
+// Back-off per role (ns between probes).
+constexpr uint32_t kSleepProducer = 256;
+constexpr uint32_t kSleepIssuer = 64;
+constexpr uint32_t kSleepEpilogue = 32;
 
 // ----------------------------------------------------------------------------
 // async proxy fences, TMA
@@ -261,6 +286,17 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads
 }
 
 __device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31u) == 0; }
+
+// Shared-memory fp32 add without a returned value, on a 32-bit shared address.
+__device__ __forceinline__ void red_shared_add(uint32_t addr, float v) {
+    asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+    return v;
+}
 
 // max(a, b, c) in one instruction (three-input form of max.f32, sm_100+).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {

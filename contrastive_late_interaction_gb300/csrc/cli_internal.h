@@ -118,6 +118,12 @@ struct MaxSimBwdLaunch {
 };
 cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream);
 
+// bf16 [rows x cols] (row stride ld elements) as a TMA map with boxes of
+// box_cols x box_rows, optionally with the 128-byte swizzle; out-of-range
+// elements read as zero.
+bool encode_bf16_tiles(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t ld, uint32_t box_cols,
+                       uint32_t box_rows, bool swizzle128);
+
 // Shared validation kernels.
 cudaError_t launch_validate_edges(const EdgeSet &set, int n, int id_limit, int32_t *status, cudaStream_t stream);
 cudaError_t launch_validate_tape(const uint64_t *offsets, int count, uint64_t rows, int32_t *status,

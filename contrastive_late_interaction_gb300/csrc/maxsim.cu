@@ -143,13 +143,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const uint32_t d0 = P.chunk_doc[chunk], d1 = P.chunk_doc[chunk + 1];
                 if (d0 == d1) continue;
                 const long long r_lo = static_cast<long long>(P.d_off[d0]), r_hi = static_cast<long long>(P.d_off[d1]);
-                if (!mbar_wait(&bar.q_free, (it & 1) ^ 1, abort_flag, P.status)) break;
+                if (!mbar_wait(&bar.q_free, (it & 1) ^ 1, abort_flag, P.status, kSleepProducer)) break;
                 ++it;
                 mbar_arrive_expect_tx(&bar.q_full, stage_bytes);
                 for (int kc = 0; kc < P.nk; ++kc)
                     tma_load_2d(q_smem + kc * BOX_BYTES, &tmap_q, &bar.q_full, kc * BK, mb * BM);
                 for (long long r0 = r_lo; r0 < r_hi; r0 += BN) {
-                    if (!mbar_wait(&bar.empty[stage], phase ^ 1, abort_flag, P.status)) { ok = false; break; }
+                    if (!mbar_wait(&bar.empty[stage], phase ^ 1, abort_flag, P.status, kSleepProducer)) { ok = false; break; }
                     mbar_arrive_expect_tx(&bar.full[stage], stage_bytes);
                     uint8_t *dst = ring + static_cast<size_t>(stage) * stage_bytes;
                     for (int kc = 0; kc < P.nk; ++kc)
@@ -176,12 +176,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const uint32_t d0 = P.chunk_doc[chunk], d1 = P.chunk_doc[chunk + 1];
                 if (d0 == d1) continue;
                 const long long r_lo = static_cast<long long>(P.d_off[d0]), r_hi = static_cast<long long>(P.d_off[d1]);
-                if (!mbar_wait(&bar.q_full, it & 1, abort_flag, P.status)) break;
+                if (!mbar_wait(&bar.q_full, it & 1, abort_flag, P.status, kSleepIssuer)) break;
                 ++it;
                 for (long long r0 = r_lo; r0 < r_hi; r0 += BN, ++tc) {
                     const uint32_t buf = tc & 1;
-                    if (!mbar_wait(&bar.full[stage], phase, abort_flag, P.status)) { ok = false; break; }
-                    if (!mbar_wait(&bar.s_free[buf], ((tc >> 1) & 1) ^ 1, abort_flag, P.status)) { ok = false; break; }
+                    if (!mbar_wait(&bar.full[stage], phase, abort_flag, P.status, kSleepIssuer)) { ok = false; break; }
+                    if (!mbar_wait(&bar.s_free[buf], ((tc >> 1) & 1) ^ 1, abort_flag, P.status, kSleepIssuer)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t da = ra + stage * stage_bytes;
                     for (int kc = 0; kc < P.nk; ++kc) {
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             int best_col = 0;
             for (int r0 = 0; r0 < span; r0 += BN, ++tc) {
                 const uint32_t buf = tc & 1;
-                if (!mbar_wait(&bar.s_full[buf], (tc >> 1) & 1, abort_flag, P.status)) { ok = false; break; }
+                if (!mbar_wait(&bar.s_full[buf], (tc >> 1) & 1, abort_flag, P.status, kSleepEpilogue)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll 1
                 for (int ch = 0; ch < BN / 32; ++ch) {
@@ -418,79 +418,189 @@ __global__ void __launch_bounds__(256) dq_kernel(MaxSimBwdLaunch L) {
     }
 }
 
-// dD rows of one document and one 64-feature slice: a window of up to
-// kDdWindow document rows accumulates in shared memory (fp32).  Each warp takes
-// 32 query rows at a time: lane j loads row j's argmax entry and c(q, d), then
-// the warp walks the 32 rows with lanes as features (lane l adds features l and
-// l + 32 of the row), so the loads of a query row are coalesced and the shared
-// adds of one instruction hit 32 consecutive words.  The window test is
-// warp-uniform.
-constexpr int kDdWindow = 512;
-constexpr int kDdThreads = 512;
-constexpr int kDdUnroll = 8;
-__global__ void __launch_bounds__(kDdThreads, 1) dd_kernel(MaxSimBwdLaunch L) {
-    extern __shared__ float dd_acc[];      // [kDdWindow][64]
+// dD rows of one document by sort-then-gather.  For a window of up to
+// kDsMaxRows document rows and a chunk of up to kDsChunk query rows:
+//   1. count, per document row s, the query rows whose argmax names it
+//      (shared-memory histogram), and scan the counts into bucket offsets;
+//   2. scatter the query rows into their buckets (a shared list of 16-bit
+//      row offsets);
+//   3. warps take document rows dynamically and sum c(q(t), d) * Q[t] over the
+//      row's bucket in registers, lanes as features (coalesced row gathers
+//      from the L2-resident query tape), then write the row once (the first
+//      chunk stores, later chunks add; the CTA owns the document, so no
+//      atomics touch dD).
+// No floating-point atomics; results do not depend on scheduling order within
+// a bucket because each bucket is summed by one warp in list order, and the
+// list order is the scatter order (atomic slot claims), which may vary between
+// runs: dD is reproducible to rounding, not bit for bit.
+constexpr int kDsThreads = 512;
+constexpr int kDsMaxRows = 4096;
+constexpr int kDsChunk = 32768;
+constexpr int kDsMaxTable = 4096;
+
+__host__ __device__ inline size_t ds_smem_bytes() {
+    return static_cast<size_t>(kDsMaxRows) * 4 + (kDsMaxRows + 1) * 4 + kDsChunk * 2 + kDsMaxTable * 4 + 64;
+}
+
+// NB: 128-feature blocks of the width (ceil(width / 128)); kDsUnroll: entry
+// pairs in flight per warp.
+template <int NB, int kDsUnroll>
+__global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch L) {
+    extern __shared__ uint8_t ds_raw[];
+    uint32_t *cnt = reinterpret_cast<uint32_t *>(ds_raw);            // [kDsMaxRows] counts, then cursors
+    uint32_t *off = cnt + kDsMaxRows;                                  // [kDsMaxRows + 1] bucket starts
+    uint16_t *list = reinterpret_cast<uint16_t *>(off + kDsMaxRows + 1);  // [kDsChunk]
+    float *ctab = reinterpret_cast<float *>(list + kDsChunk);          // [kDsMaxTable]
+    uint32_t *next_row = reinterpret_cast<uint32_t *>(ctab + kDsMaxTable);
+    __shared__ uint32_t warp_sums[kDsThreads / 32];
     if (read_status(L.status) != 0) return;
     const int d = blockIdx.x;
-    const int f0 = blockIdx.y * 64;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    constexpr int kWarps = kDdThreads / 32;
     const uint64_t o0 = L.d_off[d];
-    const long long dl = static_cast<long long>(L.d_off[d + 1] - o0);
+    const int dl = static_cast<int>(L.d_off[d + 1] - o0);
     const int32_t *am = L.argmax + static_cast<long long>(d) * L.ld_argmax;
-    const bool f_lo = f0 + lane < L.width, f_hi = f0 + 32 + lane < L.width;
-    for (long long w0 = 0; w0 < dl; w0 += kDdWindow) {
-        const int wrows = static_cast<int>(dl - w0 < kDdWindow ? dl - w0 : kDdWindow);
-        for (int i = threadIdx.x; i < wrows * 64; i += kDdThreads) dd_acc[i] = 0.f;
-        __syncthreads();
-        for (int t0 = warp * 32; t0 < L.rows_q; t0 += kWarps * 32) {
-            const int t = t0 + lane;
-            int a_l = -1;
-            float c_l = 0.f;
-            if (t < L.rows_q) {
-                a_l = __ldg(am + t);
-                if (a_l < 0 || a_l >= dl) {
+    const bool use_table = L.nq <= kDsMaxTable;
+    if (use_table)
+        for (int q = threadIdx.x; q < L.nq; q += kDsThreads) {
+            float c = L.d_scores[static_cast<long long>(q) * L.ld_ds + d];
+            if (L.mean) c /= static_cast<float>(L.q_off[q + 1] - L.q_off[q]);
+            ctab[q] = c;
+        }
+    for (int w0 = 0; w0 < dl; w0 += kDsMaxRows) {
+        const int wrows = min(kDsMaxRows, dl - w0);
+        for (int c0 = 0; c0 < L.rows_q; c0 += kDsChunk) {
+            const int crows = min(kDsChunk, L.rows_q - c0);
+            for (int r = threadIdx.x; r < wrows; r += kDsThreads) cnt[r] = 0;
+            if (threadIdx.x == 0) *next_row = 0;
+            __syncthreads();
+            // 1. histogram of the chunk's targets inside the window
+            for (int k = threadIdx.x; k < crows; k += kDsThreads) {
+                const int a = __ldg(am + c0 + k);
+                if (a < 0 || a >= dl) {
                     report(L.status, CLI_MALFORMED);
-                    a_l = -1;
-                } else {
-                    const int q = __ldg(L.qmap + t);
-                    c_l = __ldg(L.d_scores + static_cast<long long>(q) * L.ld_ds + d);
-                    if (L.mean) c_l /= static_cast<float>(L.q_off[q + 1] - L.q_off[q]);
+                    continue;
                 }
-                const long long ar = static_cast<long long>(a_l) - w0;
-                if (a_l >= 0 && (ar < 0 || ar >= wrows)) a_l = -1;    // outside this window
+                const int r = a - w0;
+                if (r >= 0 && r < wrows) atomicAdd(&cnt[r], 1u);
             }
-            const int jmax = min(32, L.rows_q - t0);
-            for (int j0 = 0; j0 < jmax; j0 += kDdUnroll) {
-                uint16_t x0[kDdUnroll], x1[kDdUnroll];
-                int a[kDdUnroll];
-                float c[kDdUnroll];
+            __syncthreads();
+            // exclusive scan of cnt[0..wrows) into off[], then cnt[] becomes the cursor
+            {
+                constexpr int kPer = kDsMaxRows / kDsThreads;   // 8 entries per thread
+                uint32_t v[kPer], sum = 0;
 #pragma unroll
-                for (int u = 0; u < kDdUnroll; ++u) {
-                    const int j = j0 + u;
-                    a[u] = __shfl_sync(0xffffffffu, a_l, j & 31);
-                    c[u] = __shfl_sync(0xffffffffu, c_l, j & 31);
-                    if (j >= jmax) a[u] = -1;
-                    const uint16_t *src = L.q + static_cast<long long>(t0 + j) * L.width + f0;
-                    x0[u] = (a[u] >= 0 && f_lo) ? __ldg(src + lane) : 0;
-                    x1[u] = (a[u] >= 0 && f_hi) ? __ldg(src + 32 + lane) : 0;
+                for (int i = 0; i < kPer; ++i) {
+                    const int r = threadIdx.x * kPer + i;
+                    v[i] = r < wrows ? cnt[r] : 0u;
+                    sum += v[i];
                 }
+                uint32_t x = sum;
 #pragma unroll
-                for (int u = 0; u < kDdUnroll; ++u) {
-                    if (a[u] >= 0) {
-                        float *row = dd_acc + (static_cast<long long>(a[u]) - w0) * 64;
-                        atomicAdd(row + lane, c[u] * __uint_as_float(static_cast<uint32_t>(x0[u]) << 16));
-                        atomicAdd(row + 32 + lane, c[u] * __uint_as_float(static_cast<uint32_t>(x1[u]) << 16));
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += y;
+                }
+                if (lane == 31) warp_sums[warp] = x;
+                __syncthreads();
+                uint32_t before = 0;
+                for (int w = 0; w < warp; ++w) before += warp_sums[w];
+                uint32_t run = before + x - sum;
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    const int r = threadIdx.x * kPer + i;
+                    if (r < wrows) {
+                        off[r] = run;
+                        cnt[r] = run;
+                    }
+                    run += v[i];
+                }
+                if (threadIdx.x == kDsThreads - 1) off[wrows] = run;
+            }
+            __syncthreads();
+            // 2. scatter the chunk's rows into their buckets
+            for (int k = threadIdx.x; k < crows; k += kDsThreads) {
+                const int a = __ldg(am + c0 + k);
+                const int r = a - w0;
+                if (a >= 0 && a < dl && r >= 0 && r < wrows) list[atomicAdd(&cnt[r], 1u)] = static_cast<uint16_t>(k);
+            }
+            __syncthreads();
+            // 3. one warp per document row at a time: sum c * Q[t] over the bucket.
+            //    Each half-warp takes one bucket entry (16 lanes x 16 bytes cover
+            //    128 features per block), kDsUnroll entry pairs per iteration.
+            const int half = lane >> 4, part = lane & 15;
+            for (;;) {
+                uint32_t r = 0;
+                if (lane == 0) r = atomicAdd(next_row, 1u);
+                r = __shfl_sync(0xffffffffu, r, 0);
+                if (r >= static_cast<uint32_t>(wrows)) break;
+                float acc[NB][8];
+#pragma unroll
+                for (int k = 0; k < NB; ++k)
+#pragma unroll
+                    for (int i2 = 0; i2 < 8; ++i2) acc[k][i2] = 0.f;
+                const uint32_t b0 = off[r], b1 = off[r + 1];
+                for (uint32_t e = b0; e < b1; e += 2 * kDsUnroll) {
+                    uint4 x[kDsUnroll][NB];
+                    float c[kDsUnroll];
+#pragma unroll
+                    for (int u = 0; u < kDsUnroll; ++u) {
+                        const uint32_t ee = e + 2 * u + half;
+                        const bool v = ee < b1;
+                        const int t = c0 + (v ? list[ee] : 0);
+                        const int q = __ldg(L.qmap + t);
+                        float cc;
+                        if (use_table) {
+                            cc = ctab[q];
+                        } else {
+                            cc = __ldg(L.d_scores + static_cast<long long>(q) * L.ld_ds + d);
+                            if (L.mean) cc /= static_cast<float>(L.q_off[q + 1] - L.q_off[q]);
+                        }
+                        c[u] = v ? cc : 0.f;
+                        const uint16_t *src = L.q + static_cast<long long>(t) * L.width;
+#pragma unroll
+                        for (int k = 0; k < NB; ++k) {
+                            const int f = k * 128 + part * 8;
+                            x[u][k] = (v && f < L.width) ? __ldg(reinterpret_cast<const uint4 *>(src + f))
+                                                         : make_uint4(0, 0, 0, 0);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < kDsUnroll; ++u)
+#pragma unroll
+                        for (int k = 0; k < NB; ++k) {
+                            float xv[8];
+                            bf16x8_to_f32(x[u][k], xv);
+#pragma unroll
+                            for (int i2 = 0; i2 < 8; ++i2) acc[k][i2] = fmaf(c[u], xv[i2], acc[k][i2]);
+                        }
+                }
+                // combine the two half-warps, then half 0 writes the row
+#pragma unroll
+                for (int k = 0; k < NB; ++k)
+#pragma unroll
+                    for (int i2 = 0; i2 < 8; ++i2) acc[k][i2] += __shfl_xor_sync(0xffffffffu, acc[k][i2], 16);
+                if (half == 0) {
+                    float *dst = L.dd + (static_cast<long long>(o0) + w0 + r) * L.width;
+#pragma unroll
+                    for (int k = 0; k < NB; ++k) {
+                        const int f = k * 128 + part * 8;
+                        if (f < L.width) {
+                            float4 lo = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+                            float4 hi = make_float4(acc[k][4], acc[k][5], acc[k][6], acc[k][7]);
+                            if (c0 > 0) {
+                                const float4 ol = reinterpret_cast<const float4 *>(dst + f)[0];
+                                const float4 oh = reinterpret_cast<const float4 *>(dst + f)[1];
+                                lo.x += ol.x; lo.y += ol.y; lo.z += ol.z; lo.w += ol.w;
+                                hi.x += oh.x; hi.y += oh.y; hi.z += oh.z; hi.w += oh.w;
+                            }
+                            reinterpret_cast<float4 *>(dst + f)[0] = lo;
+                            reinterpret_cast<float4 *>(dst + f)[1] = hi;
+                        }
                     }
                 }
             }
+            __syncthreads();
         }
-        __syncthreads();
-        for (int i = threadIdx.x; i < wrows * 64; i += kDdThreads) {
-            const int r = i >> 6, f = i & 63;
-            if (f0 + f < L.width) L.dd[(static_cast<long long>(o0) + w0 + r) * L.width + f0 + f] = dd_acc[i];
-        }
-        __syncthreads();
     }
 }
 
@@ -556,12 +666,18 @@ cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream
         default: dq_kernel<4><<<dq_grid, 256, 0, stream>>>(L); break;
     }
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    const size_t dd_smem = static_cast<size_t>(kDdWindow) * 64 * sizeof(float);
-    if ((err = cudaFuncSetAttribute(dd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(dd_smem))) != cudaSuccess)
-        return err;
-    dim3 grid(L.nd, (L.width + 63) / 64);
-    dd_kernel<<<grid, kDdThreads, dd_smem, stream>>>(L);
+    const size_t ds_smem = ds_smem_bytes();
+    if ((L.width + 127) / 128 == 1) {
+        if ((err = cudaFuncSetAttribute(dd_sort_kernel<1, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(ds_smem))) != cudaSuccess)
+            return err;
+        dd_sort_kernel<1, 8><<<L.nd, kDsThreads, ds_smem, stream>>>(L);
+    } else {
+        if ((err = cudaFuncSetAttribute(dd_sort_kernel<2, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(ds_smem))) != cudaSuccess)
+            return err;
+        dd_sort_kernel<2, 3><<<L.nd, kDsThreads, ds_smem, stream>>>(L);
+    }
     return cudaGetLastError();
 }
 

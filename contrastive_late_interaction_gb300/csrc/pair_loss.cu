@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const bool diag = I == J;
                 for (int pass = 0; pass < 2 && ok; ++pass) {   // S pass, then the dE pass
                     for (int kc = 0; kc < P.nk; ++kc) {
-                        if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag, P.status)) { ok = false; break; }
+                        if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag, P.status, kSleepProducer)) { ok = false; break; }
                         mbar_arrive_expect_tx(&sm.full[stage], diag ? BOX_BYTES : 2 * BOX_BYTES);
                         tma_load_2d(sm.ring[stage][0], &tmap_e, &sm.full[stage], kc * BK, I * BM);
                         if (!diag) tma_load_2d(sm.ring[stage][1], &tmap_e, &sm.full[stage], kc * BK, J * BM);
@@ -202,10 +202,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 decode_pair(p, P.nb, I, J);
                 const bool diag = I == J;
                 // S = E_I E_J^T
-                if (!mbar_wait(&sm.s_free, (k & 1) ^ 1, abort_flag, P.status)) break;
+                if (!mbar_wait(&sm.s_free, (k & 1) ^ 1, abort_flag, P.status, kSleepIssuer)) break;
                 tc_fence_after();
                 for (int kc = 0; kc < P.nk; ++kc) {
-                    if (!mbar_wait(&sm.full[stage], phase, abort_flag, P.status)) { ok = false; break; }
+                    if (!mbar_wait(&sm.full[stage], phase, abort_flag, P.status, kSleepIssuer)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a = smem_u32(sm.ring[stage][0]);
                     const uint32_t b = diag ? a : smem_u32(sm.ring[stage][1]);
@@ -219,11 +219,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (!ok) break;
                 mma_commit(&sm.s_full);
                 // dE_I += H E_J, dE_J += H^T E_I, 64 columns of D at a time
-                if (!mbar_wait(&sm.h_ready, k & 1, abort_flag, P.status)) break;
+                if (!mbar_wait(&sm.h_ready, k & 1, abort_flag, P.status, kSleepIssuer)) break;
                 tc_fence_after();
                 for (int dc = 0; dc < P.nk; ++dc, ++chunk) {
-                    if (!mbar_wait(&sm.full[stage], phase, abort_flag, P.status)) { ok = false; break; }
-                    if (!mbar_wait(&sm.de_free, (chunk & 1) ^ 1, abort_flag, P.status)) { ok = false; break; }
+                    if (!mbar_wait(&sm.full[stage], phase, abort_flag, P.status, kSleepIssuer)) { ok = false; break; }
+                    if (!mbar_wait(&sm.de_free, (chunk & 1) ^ 1, abort_flag, P.status, kSleepIssuer)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t ei = smem_u32(sm.ring[stage][0]);
                     const uint32_t ej = diag ? ei : smem_u32(sm.ring[stage][1]);
@@ -284,8 +284,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 e_beg = lo;
             }
-            if (!mbar_wait(&sm.s_full, k & 1, abort_flag, P.status)) break;
-            if (!mbar_wait(&sm.h_free, (k & 1) ^ 1, abort_flag, P.status)) break;
+            if (!mbar_wait(&sm.s_full, k & 1, abort_flag, P.status, kSleepEpilogue)) break;
+            if (!mbar_wait(&sm.h_free, (k & 1) ^ 1, abort_flag, P.status, kSleepEpilogue)) break;
             tc_fence_after();
 
             float acc_sp = 0.f, acc_p = 0.f, acc_ps = 0.f;     // default cells (times 2 w_d later)
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             // Drain the gradient chunks into dE.
             bool ok = true;
             for (int dc = 0; dc < P.nk; ++dc, ++chunk) {
-                if (!mbar_wait(&sm.de_full, chunk & 1, abort_flag, P.status)) { ok = false; break; }
+                if (!mbar_wait(&sm.de_full, chunk & 1, abort_flag, P.status, kSleepEpilogue)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll 1
                 for (int side = 0; side < (diag ? 1 : 2); ++side) {
