@@ -71,12 +71,17 @@ struct Params {
 // the current document.  Keys carry 31 - column in the 5 low mantissa bits, so
 // the max of the keys names the lowest column among equal values; the tree
 // uses the three-input max (16 instructions for 32 keys).
+// Each key is (bits & hi_mask) | (31 - r), one lop3 with the mask (~31) held
+// in a register so the two-constant form does not split into two operations.
 template <bool kFull>
-__device__ __forceinline__ void chunk_max(const float (&v)[32], int lo, int hi, int base, float &best, int &best_col) {
+__device__ __forceinline__ void chunk_max(const float (&v)[32], int lo, int hi, int base, float &best, int &best_col,
+                                          uint32_t hi_mask) {
     float key[32];
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
-        const float k = __int_as_float((__float_as_int(v[r]) & ~31) | (31 - r));
+        uint32_t kb;
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(kb) : "r"(__float_as_uint(v[r])), "r"(hi_mask), "r"(31 - r));
+        const float k = __uint_as_float(kb);
         key[r] = kFull ? k : ((r >= lo && r < hi) ? k : -INFINITY);
     }
     float m[12];
@@ -206,6 +211,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        uint32_t hi_mask;
+        asm volatile("mov.b32 %0, 0xFFFFFFE0;" : "=r"(hi_mask));   // opaque to constant folding
         uint32_t tc = 0;
         bool ok = true;
         for (long long w = blockIdx.x; w < P.items && ok; w += gridDim.x) {
@@ -225,6 +232,32 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const uint32_t buf = tc & 1;
                 if (!mbar_wait(&bar.s_full[buf], (tc >> 1) & 1, abort_flag, P.status, kSleepEpilogue)) { ok = false; break; }
                 tc_fence_after();
+                if (r0 + BN <= span && cur_end >= r0 + BN) {
+                    // the whole tile lies inside the current document
+#pragma unroll 1
+                    for (int ch = 0; ch < BN / 32; ++ch) {
+                        float v[32];
+                        tmem_ld32(tmem + lane_base + buf * BN + ch * 32, v);
+                        chunk_max<true>(v, 0, 32, r0 + ch * 32 - cur_beg, best, best_col, hi_mask);
+                    }
+                    if (cur_end == r0 + BN) {
+                        if (t_ok) {
+                            P.argmax[static_cast<long long>(cur) * P.ld_argmax + t] = best_col;
+                            P.mval[static_cast<long long>(cur) * P.rows_q + t] = best;
+                        }
+                        ++cur;
+                        best = -INFINITY;
+                        best_col = 0;
+                        if (cur < d1) {
+                            cur_beg = cur_end;
+                            cur_end = static_cast<int>(static_cast<long long>(P.d_off[cur + 1]) - r_lo);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar.s_free[buf]);
+                    continue;
+                }
 #pragma unroll 1
                 for (int ch = 0; ch < BN / 32; ++ch) {
                     const int c0 = r0 + ch * 32;
@@ -234,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const int hi_chunk = min(c0 + 32, span);
                     if (hi_chunk == c0 + 32 && cur_end >= c0 + 32) {
                         // the whole chunk lies inside the current document
-                        chunk_max<true>(v, 0, 32, c0 - cur_beg, best, best_col);
+                        chunk_max<true>(v, 0, 32, c0 - cur_beg, best, best_col, hi_mask);
                         if (cur_end == c0 + 32) {
                             if (t_ok) {
                                 P.argmax[static_cast<long long>(cur) * P.ld_argmax + t] = best_col;
@@ -253,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     int lo = c0;
                     while (lo < hi_chunk) {   // warp-uniform: document boundaries are shared by all rows
                         const int seg_hi = min(hi_chunk, cur_end);
-                        chunk_max<false>(v, lo - c0, seg_hi - c0, c0 - cur_beg, best, best_col);
+                        chunk_max<false>(v, lo - c0, seg_hi - c0, c0 - cur_beg, best, best_col, hi_mask);
                         if (seg_hi == cur_end) {
                             if (t_ok) {
                                 P.argmax[static_cast<long long>(cur) * P.ld_argmax + t] = best_col;
