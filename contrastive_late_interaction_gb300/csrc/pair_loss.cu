@@ -52,6 +52,7 @@ constexpr uint32_t TM_S = 0, TM_DEI = 128, TM_DEJ = 192;
 struct SharedStorage {
     alignas(1024) uint8_t ring[STAGES][2][BOX_BYTES];
     alignas(1024) uint8_t h[2][BOX_BYTES];     // H tile, two 64-column K blocks
+    alignas(16) float stage_t[4][32 * 16];     // per epilogue warp: 32 rows x 16 fp32, transposed drain
     uint64_t full[STAGES], empty[STAGES];
     uint64_t s_full, s_free, h_ready, h_free, de_full, de_free, mma_done;
     uint32_t tmem_base;
@@ -74,18 +75,62 @@ struct Params {
     int32_t *status;
 };
 
-// Tile pair p -> (I, J), I <= J, enumerated row by row over the upper triangle.
+// Tile pair p -> (I, J), I <= J.  The upper triangle of tile pairs is walked in
+// super-blocks of kSuper x kSuper tiles (row-major over super-blocks I' <= J',
+// then row-major inside a super-block, keeping I <= J on the diagonal ones),
+// so the CTAs running at the same time read and reduce into the rows of a few
+// super-blocks only: their E rows and dE rows stay resident in L2.
+constexpr int kSuper = 8;
+
+// Row-major enumeration of the upper triangle of an n x n grid: index -> (i, j).
+__device__ __forceinline__ void tri_decode(long long p, int n, int &i, int &j) {
+    // start(i) = i*n - i*(i-1)/2; invert approximately, then correct.
+    const double fn = static_cast<double>(n) + 0.5;
+    int r = static_cast<int>(fn - sqrt(fn * fn - 2.0 * static_cast<double>(p)));
+    if (r < 0) r = 0;
+    if (r > n - 1) r = n - 1;
+    auto start = [n](long long x) { return x * n - x * (x - 1) / 2; };
+    while (r > 0 && start(r) > p) --r;
+    while (r < n - 1 && start(r + 1) <= p) ++r;
+    i = r;
+    j = r + static_cast<int>(p - start(r));
+}
+
 __device__ __forceinline__ void decode_pair(long long p, int nb, int &I, int &J) {
-    // start(I) = I*nb - I*(I-1)/2; invert approximately, then correct.
-    double fnb = static_cast<double>(nb) + 0.5;
-    int i = static_cast<int>(fnb - sqrt(fnb * fnb - 2.0 * static_cast<double>(p)));
-    if (i < 0) i = 0;
-    if (i > nb - 1) i = nb - 1;
-    auto start = [nb](long long r) { return r * nb - r * (r - 1) / 2; };
-    while (i > 0 && start(i) > p) --i;
-    while (i < nb - 1 && start(i + 1) <= p) ++i;
-    I = i;
-    J = i + static_cast<int>(p - start(i));
+    const int ns = (nb + kSuper - 1) / kSuper;          // super-blocks per side
+    const int last = nb - (ns - 1) * kSuper;            // tiles in the last super-block row/column
+    // walk super-blocks (si, sj), si <= sj, counting the tile pairs each holds
+    long long before = 0;
+    for (int si = 0; si < ns; ++si) {
+        const int hi = si == ns - 1 ? last : kSuper;
+        // off-diagonal super-blocks of this row: (ns - 1 - si) of them, the last one narrower
+        const long long diag = static_cast<long long>(hi) * (hi + 1) / 2;
+        const long long full_off = si < ns - 1 ? static_cast<long long>(ns - 2 - si) * hi * kSuper + static_cast<long long>(hi) * last : 0;
+        if (p < before + diag + full_off) {
+            long long q = p - before;
+            if (q < diag) {   // diagonal super-block: upper triangle of hi x hi
+                int i, j;
+                tri_decode(q, hi, i, j);
+                I = si * kSuper + i;
+                J = si * kSuper + j;
+                return;
+            }
+            q -= diag;
+            // off-diagonal super-blocks sj = si+1 .. ns-1, each hi x width(sj), row-major
+            for (int sj = si + 1; sj < ns; ++sj) {
+                const int w = sj == ns - 1 ? last : kSuper;
+                const long long cnt = static_cast<long long>(hi) * w;
+                if (q < cnt) {
+                    I = si * kSuper + static_cast<int>(q / w);
+                    J = sj * kSuper + static_cast<int>(q % w);
+                    return;
+                }
+                q -= cnt;
+            }
+        }
+        before += diag + full_off;
+    }
+    I = J = nb - 1;   // not reached for p < tile_pairs
 }
 
 __device__ __forceinline__ float fast_ex2(float x) {
@@ -265,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float c_h = t * inv_n;             // H = (t/N) G
         const float w_d = P.named ? 0.0f : P.ambient;
         const uint32_t h0 = smem_u32(sm.h[0]);
+        const uint32_t stage_s = smem_u32(sm.stage_t[quad]);
         uint32_t k = 0, chunk = 0;
         for (long long p = blockIdx.x; p < P.tile_pairs; p += gridDim.x, ++k) {
             int I, J;
@@ -372,17 +418,34 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tc_fence_after();
 #pragma unroll 1
                 for (int side = 0; side < (diag ? 1 : 2); ++side) {
-                    const int grow = (side == 0 ? I : J) * BM + row;
+                    const int row0 = (side == 0 ? I : J) * BM + quad * 32;   // first row of this warp's 32
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         float v[32];
                         tmem_ld32(tmem + lane_base + (side == 0 ? TM_DEI : TM_DEJ) + half * 32, v);
                         const int col0 = dc * BK + half * 32;
-                        if (grow < P.n) {
-                            float *dst = P.d_e + static_cast<long long>(grow) * P.ld_de + col0;
 #pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                if (col0 + q * 4 < P.width) red_add_v4(dst + q * 4, v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+                        for (int h16 = 0; h16 < 2; ++h16) {
+                            // lane = row: write 16 values (4 x 16 B, chunk index swizzled by row)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const int kk = k ^ ((lane >> 1) & 3);
+                                st_shared_v4(stage_s + (lane * 16 + kk * 4) * 4, __float_as_uint(v[h16 * 16 + k * 4]),
+                                             __float_as_uint(v[h16 * 16 + k * 4 + 1]), __float_as_uint(v[h16 * 16 + k * 4 + 2]),
+                                             __float_as_uint(v[h16 * 16 + k * 4 + 3]));
+                            }
+                            __syncwarp();
+                            // read back: instruction m covers rows 8m .. 8m+7, 4 lanes x 16 B per row
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) {
+                                const int r = m * 8 + (lane >> 2), k = lane & 3;
+                                const int kk = k ^ ((r >> 1) & 3);
+                                const float4 x = *reinterpret_cast<const float4 *>(&sm.stage_t[quad][r * 16 + kk * 4]);
+                                const int grow = row0 + r, gcol = col0 + h16 * 16 + k * 4;
+                                if (grow < P.n && gcol < P.width)
+                                    red_add_v4(P.d_e + static_cast<long long>(grow) * P.ld_de + gcol, x.x, x.y, x.z, x.w);
+                            }
+                            __syncwarp();
                         }
                     }
                 }
