@@ -403,12 +403,20 @@ def dist_setup(args):
 
 
 def max_over_ranks(pg, value, device):
+    """The slowest rank's value (every rank gets it); `pg` is torch.distributed or None."""
     if pg is None:
         return value
     import torch
     t = torch.tensor([value], dtype=torch.float64, device=device)
     pg.all_reduce(t, op=pg.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(pg, world, flops_per_rank, ms_local, device):
+    """Weak scaling: every rank runs its own batch of `flops_per_rank`; the job's time is the slowest
+    rank's, and its throughput is all ranks' work over that time.  Returns (ms, TFLOP/s)."""
+    ms = max_over_ranks(pg, ms_local, device)
+    return ms, world * flops_per_rank / (ms * 1e-3) / 1e12
 
 
 def run_reference(args, world, rank):
@@ -437,9 +445,12 @@ def run_reference(args, world, rank):
 
 def main():
     args = parse_args()
-    world, rank, local, pg = dist_setup(args)
     if args.impl == "reference":
+        # The oracle runs on rank 0's host cores only; other ranks exit at once, without a process group.
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
         return run_reference(args, world, rank)
+    world, rank, local, pg = dist_setup(args)
     import torch
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
@@ -479,13 +490,10 @@ def main():
         pg.barrier()
     step_ms = [s.elapsed_time(e) for s, e in st_ev]
     part_ms = {n: [ev[k][n][0].elapsed_time(ev[k][n][1]) for k in range(args.steps)] for n in names}
-    ms = statistics.mean(step_ms)
-    ms = max_over_ranks(pg, ms, device)
-
     p, m = step.p, step.m
     flops = (pooled_flops(p) if p is not None else 0.0) + \
             ((maxsim_fwd_flops(m) + maxsim_bwd_flops(m)) if m is not None else 0.0)
-    value = world * flops / (ms * 1e-3) / 1e12
+    ms, value = aggregate(pg, world, flops, statistics.mean(step_ms), device)
     burst, sustained, hbm, peak_src = peaks()
     parts = {}
     if p is not None:
