@@ -55,12 +55,15 @@ def _load():
                                                      I64, P, P, P, P, P, P, I]
             lib.oracle_pair_loss_sigmoid_scores.argtypes = [I64, I64, P, D, D, P, P, P, P, P, P, P, P, P,
                                                             I, D, P, P, P, P]
+            lib.oracle_pair_loss_scores_form.argtypes = [I, I64, I64, P, D, D, P, P, P, P, P, P, P, P, P,
+                                                         I, D, P, P, P, P]
             lib.oracle_maxsim_pairs.argtypes = [I64, P, P, I64, P, P, I64, I, I64, P, P, P, P, P, P, I]
             lib.oracle_maxsim_forward.argtypes = [I64, P, P, I64, P, P, I64, I, P, P, P, I]
             lib.oracle_maxsim_backward.argtypes = [I64, P, P, I64, P, P, I64, I, P, P, P, P, I]
             lib.oracle_maxsim_grad_query.argtypes = [I64, P, P, I64, P, P, I64, I, I64, P, P]
             lib.oracle_maxsim_grad_doc.argtypes = [I64, P, P, I64, P, P, I64, I, I64, P, P]
-            for f in ("oracle_pair_loss_sigmoid", "oracle_pair_loss_sigmoid_scores", "oracle_maxsim_pairs",
+            for f in ("oracle_pair_loss_sigmoid", "oracle_pair_loss_sigmoid_scores", "oracle_pair_loss_scores_form",
+                      "oracle_maxsim_pairs",
                       "oracle_maxsim_forward", "oracle_maxsim_backward", "oracle_maxsim_grad_query",
                       "oracle_maxsim_grad_doc"):
                 getattr(lib, f).restype = I
@@ -153,6 +156,30 @@ def pair_loss_sigmoid_scores(scores, t, b, attract=None, repel=None, ignore=None
                                              _ptr(ro), _ptr(ri), _ptr(rw), _ptr(io), _ptr(ii), _ptr(sd),
                                              int(negatives_named), float(ambient_weight), _ptr(out[0:1]),
                                              _ptr(ds), _ptr(out[1:2]), _ptr(out[2:3]))
+    assert rc == 0
+    return dict(loss=out[0], dt=out[1], db=out[2], dscores=ds)
+
+
+FORMS = {"balanced": 1, "ranked": 2}
+
+
+def pair_loss_scores_form(form, scores, t, b, attract=None, repel=None, ignore=None, sides=None,
+                          negatives_named=False, ambient_weight=1.0):
+    """The `balanced` or `ranked` pair-loss form over a score matrix [R, C].  Returns dict(loss, dt, db,
+    dscores)."""
+    lib = _load()
+    s = _f64(scores)
+    r, c = s.shape
+    ao, ai, aw = _edges(attract)
+    ro, ri, rw = _edges(repel)
+    io, ii, _ = _edges(ignore)
+    sd = None if sides is None else np.ascontiguousarray(sides, dtype=np.uint8)
+    ds = np.zeros((r, c))
+    out = np.zeros(3)
+    rc = lib.oracle_pair_loss_scores_form(FORMS[form], r, c, _ptr(s), float(t), float(b), _ptr(ao), _ptr(ai),
+                                          _ptr(aw), _ptr(ro), _ptr(ri), _ptr(rw), _ptr(io), _ptr(ii), _ptr(sd),
+                                          int(negatives_named), float(ambient_weight), _ptr(out[0:1]), _ptr(ds),
+                                          _ptr(out[1:2]), _ptr(out[2:3]))
     assert rc == 0
     return dict(loss=out[0], dt=out[1], db=out[2], dscores=ds)
 

@@ -496,3 +496,99 @@ int oracle_maxsim_grad_doc(int64_t nq, const uint64_t *q_off, const double *q, i
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* the `balanced` and `ranked` pair-loss forms over a score matrix            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * "Training", `uform_pair_loss_form_t`:
+ *   balanced -- the sigmoid cross-entropy of every cell, its attract and repel
+ *               halves normalized apart;
+ *   ranked   -- the sigmoid cross-entropy of every positive's score over every
+ *               negative's, where the bias cancels.
+ * Readings (the pages give words only):
+ *   balanced: per row p, l_p = sum_{attract} w l / sum_{attract} w
+ *                            + sum_{repel} w l / sum_{repel} w,
+ *             each half present only when the row has such cells, with the
+ *             sigmoid cell loss l = softplus(-y (t S + b));
+ *   ranked:   per row p, l_p = sum_{i in P, j in N} w_i w_j softplus(-t (S_pi - S_pj))
+ *                            / sum_{i in P, j in N} w_i w_j,
+ *             P the row's attract cells, N its repel cells (explicit or ambient),
+ *             0 when either is empty;
+ *   both:     L = (1/R) sum_p l_p; relations and sides resolve cells exactly
+ *             as in oracle_pair_loss_sigmoid_scores.
+ * form: 1 = balanced, 2 = ranked (the pages' enumerator values).
+ */
+int oracle_pair_loss_scores_form(int form, int64_t r_count, int64_t c_count, const double *scores, double t,
+                                 double b, const uint64_t *att_off, const uint32_t *att_ids, const double *att_w,
+                                 const uint64_t *rep_off, const uint32_t *rep_ids, const double *rep_w,
+                                 const uint64_t *ign_off, const uint32_t *ign_ids, const uint8_t *sides,
+                                 int negatives_named, double ambient_weight, double *loss, double *dscores,
+                                 double *dt, double *db) {
+    if (r_count <= 0 || c_count <= 0 || !scores || (form != 1 && form != 2)) return 1;
+    edges_t att = {att_off, att_ids, att_w}, rep = {rep_off, rep_ids, rep_w}, ign = {ign_off, ign_ids, NULL};
+    double *y = (double *)malloc(sizeof(double) * (size_t)c_count);
+    double *w = (double *)malloc(sizeof(double) * (size_t)c_count);
+    if (!y || !w) { free(y); free(w); return 2; }
+    const double inv_r = 1.0 / (double)r_count;
+    double L = 0, T = 0, B = 0;
+    if (dscores) memset(dscores, 0, sizeof(double) * (size_t)(r_count * c_count));
+    for (int64_t i = 0; i < r_count; ++i) {
+        const double *s = scores + i * c_count;
+        double *ds = dscores ? dscores + i * c_count : NULL;
+        double wa = 0, wr = 0;
+        for (int64_t j = 0; j < c_count; ++j) {
+            y[j] = 0;
+            w[j] = 0;
+            int scored = !(sides && (!(sides[i] & 1) || !(sides[j] & 2)));
+            if (scored && resolve(&att, &rep, &ign, negatives_named, ambient_weight, i, j, &y[j], &w[j])) {
+                if (y[j] > 0) wa += w[j]; else wr += w[j];
+            } else {
+                y[j] = 0;
+                w[j] = 0;
+            }
+        }
+        if (form == 1) {
+            for (int64_t j = 0; j < c_count; ++j) {
+                if (y[j] == 0) continue;
+                const double norm = y[j] > 0 ? wa : wr;
+                double l, g;
+                cell(y[j], w[j], t * s[j] + b, &l, &g);   /* g = dl/dz */
+                L += l / norm * inv_r;
+                T += g / norm * inv_r * s[j];
+                B += g / norm * inv_r;
+                if (ds) ds[j] = t * g / norm * inv_r;
+            }
+        } else {
+            double z = 0;
+            for (int64_t a = 0; a < c_count; ++a)
+                if (y[a] > 0)
+                    for (int64_t n = 0; n < c_count; ++n)
+                        if (y[n] < 0) z += w[a] * w[n];
+            if (z <= 0) continue;
+            for (int64_t a = 0; a < c_count; ++a) {
+                if (y[a] <= 0) continue;
+                for (int64_t n = 0; n < c_count; ++n) {
+                    if (y[n] >= 0) continue;
+                    const double pw = w[a] * w[n] / z * inv_r;
+                    const double m = t * (s[a] - s[n]);
+                    /* softplus(-m) = -log sigma(m); d/dm = -sigma(-m) */
+                    L += pw * oracle_softplus(-m);
+                    const double dm = -pw * oracle_sigmoid(-m);
+                    T += dm * (s[a] - s[n]);
+                    if (ds) {
+                        ds[a] += dm * t;
+                        ds[n] -= dm * t;
+                    }
+                }
+            }
+        }
+    }
+    free(y);
+    free(w);
+    *loss = L;
+    if (dt) *dt = T;
+    if (db) *db = B;
+    return 0;
+}
