@@ -11,7 +11,7 @@ _BINDING_NAMES = {
     "UnsupportedError", "check_device_status", "device_edges", "maxsim_backward", "maxsim_backward_workspace_bytes",
     "maxsim_scores", "maxsim_workspace_bytes", "pair_loss_sigmoid_fwd_bwd", "pair_loss_sigmoid_scores_fwd_bwd",
     "pair_loss_sigmoid_scores_workspace_bytes", "pair_loss_sigmoid_workspace_bytes", "status_name", "LIB_PATH",
-    "raise_for",
+    "raise_for", "pair_loss_scores_fwd_bwd", "pair_loss_scores_workspace_bytes",
 }
 
 

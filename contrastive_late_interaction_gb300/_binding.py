@@ -93,6 +93,13 @@ class PairLossSigmoidScoresArgs(ctypes.Structure):
                 ("workspace_bytes", c_size_t), ("device_status", c_void_p), ("stream", c_void_p)]
 
 
+class PairLossScoresArgs(ctypes.Structure):
+    _fields_ = [("form", c_int), ("args", PairLossSigmoidScoresArgs)]
+
+
+FORMS = {"balanced": 1, "ranked": 2, "sigmoid": 3}
+
+
 class Tape(ctypes.Structure):
     _fields_ = [("data", c_void_p), ("offsets", c_void_p), ("count", c_size_t), ("rows", c_size_t)]
 
@@ -117,6 +124,8 @@ EXPORTS = {
     "pair_loss_sigmoid_workspace_bytes": (c_size_t, [c_size_t, c_size_t, c_size_t]),
     "pair_loss_sigmoid_scores_fwd_bwd": (c_int, [ctypes.POINTER(PairLossSigmoidScoresArgs)]),
     "pair_loss_sigmoid_scores_workspace_bytes": (c_size_t, [c_size_t, c_size_t]),
+    "pair_loss_scores_fwd_bwd": (c_int, [ctypes.POINTER(PairLossScoresArgs)]),
+    "pair_loss_scores_workspace_bytes": (c_size_t, [c_int, c_size_t, c_size_t]),
     "maxsim_scores": (c_int, [ctypes.POINTER(MaxSimArgs)]),
     "maxsim_workspace_bytes": (c_size_t, [c_size_t, c_size_t, c_size_t, c_size_t, c_size_t]),
     "maxsim_backward": (c_int, [ctypes.POINTER(MaxSimBackwardArgs)]),
@@ -274,6 +283,37 @@ def pair_loss_sigmoid_scores_fwd_bwd(scores, inverse_temperature, bias, attract,
         d_inverse_temperature=_ptr(dt), d_bias=_ptr(db), workspace=_ptr(ws), workspace_bytes=ws.numel(),
         device_status=_ptr(st), stream=_stream(stream))
     raise_for(lib.pair_loss_sigmoid_scores_fwd_bwd(ctypes.byref(args)), "pair_loss_sigmoid_scores_fwd_bwd")
+    return dict(loss=loss, d_scores=ds, d_inverse_temperature=dt, d_bias=db, device_status=st)
+
+
+def pair_loss_scores_workspace_bytes(form, rows, cols):
+    return int(lib.pair_loss_scores_workspace_bytes(FORMS[form], rows, cols))
+
+
+def pair_loss_scores_fwd_bwd(form, scores, inverse_temperature, bias, attract, repel=None, ignore=None, sides=None,
+                             negatives_named=False, ambient_weight=1.0, out=None, workspace=None, device_status=None,
+                             stream=None):
+    """Pair loss of form 'balanced', 'ranked' or 'sigmoid' over an fp32 score matrix [rows, cols]."""
+    _check_cuda(scores, "scores", torch.float32)
+    _check_cuda(sides, "sides", torch.uint8)
+    rows, cols = scores.shape
+    dev = scores.device
+    out = dict(out or {})
+    loss = out.get("loss") if out.get("loss") is not None else torch.empty(1, device=dev)
+    ds = out.get("d_scores") if out.get("d_scores") is not None else torch.empty(rows, cols, device=dev)
+    dt = out.get("d_inverse_temperature") if out.get("d_inverse_temperature") is not None else torch.empty(1, device=dev)
+    db = out.get("d_bias") if out.get("d_bias") is not None else torch.empty(1, device=dev)
+    st = device_status if device_status is not None else torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = workspace if workspace is not None else _ws(pair_loss_scores_workspace_bytes(form, rows, cols), dev)
+    A, R, I = _edges(attract, rows), _edges(repel, rows), _edges(ignore, rows)
+    inner = PairLossSigmoidScoresArgs(
+        rows=rows, cols=cols, ld=scores.stride(0), scores=_ptr(scores), inverse_temperature=_ptr(inverse_temperature),
+        bias=_ptr(bias), relations=Relations(A, R, I, int(bool(negatives_named)), float(ambient_weight)),
+        sides=_ptr(sides), loss=_ptr(loss), d_scores=_ptr(ds), ld_d_scores=ds.stride(0),
+        d_inverse_temperature=_ptr(dt), d_bias=_ptr(db), workspace=_ptr(ws), workspace_bytes=ws.numel(),
+        device_status=_ptr(st), stream=_stream(stream))
+    args = PairLossScoresArgs(form=FORMS[form], args=inner)
+    raise_for(lib.pair_loss_scores_fwd_bwd(ctypes.byref(args)), "pair_loss_scores_fwd_bwd")
     return dict(loss=loss, d_scores=ds, d_inverse_temperature=dt, d_bias=db, device_status=st)
 
 

@@ -247,6 +247,78 @@ cli_status_t pair_loss_sigmoid_scores_fwd_bwd(const cli_pair_loss_sigmoid_scores
     return CLI_OK;
 }
 
+size_t pair_loss_scores_workspace_bytes(int form, size_t rows, size_t cols) {
+    if (form == CLI_FORM_SIGMOID) return pair_loss_sigmoid_scores_workspace_bytes(rows, cols);
+    return align256(rows * 4 * sizeof(float));
+}
+
+cli_status_t pair_loss_scores_fwd_bwd(const cli_pair_loss_scores_t *f) {
+    if (!f) return CLI_INVALID_ARGUMENT;
+    if (f->form == CLI_FORM_SIGMOID) return pair_loss_sigmoid_scores_fwd_bwd(&f->args);
+    if (f->form != CLI_FORM_BALANCED && f->form != CLI_FORM_RANKED) return CLI_INVALID_ARGUMENT;
+    const cli_pair_loss_sigmoid_scores_t *a = &f->args;
+    const cli_relations_t &rel = a->relations;
+    if (!a->scores || !a->inverse_temperature || !a->bias || !a->loss || !a->d_scores || !a->d_inverse_temperature ||
+        !a->d_bias || !a->device_status || !a->workspace)
+        return CLI_INVALID_ARGUMENT;
+    if (a->rows == 0 || a->cols == 0 || a->rows >= (1ull << 31) || a->cols >= (1ull << 31)) return CLI_SHAPE_MISMATCH;
+    if (a->ld < a->cols || a->ld_d_scores < a->cols) return CLI_SHAPE_MISMATCH;
+    if (a->sides && a->rows != a->cols) return CLI_SHAPE_MISMATCH;
+    if (!edges_ok(rel.attract) || !edges_ok(rel.repel) || !edges_ok(rel.ignore)) return CLI_INVALID_ARGUMENT;
+    if (!rel.attract.offsets || rel.attract.edges == 0) return CLI_INVALID_ARGUMENT;
+    if (!(rel.ambient_weight >= 0.0f) || std::isinf(rel.ambient_weight)) return CLI_INVALID_ARGUMENT;
+    const size_t wsb = pair_loss_scores_workspace_bytes(f->form, a->rows, a->cols);
+    if (a->workspace_bytes < wsb) return CLI_INVALID_ARGUMENT;
+    const size_t r = a->rows;
+    const Range inputs[] = {
+        range_of(a->scores, ((r - 1) * a->ld + a->cols) * 4),
+        range_of(a->inverse_temperature, 4),
+        range_of(a->bias, 4),
+        range_of(a->sides, a->sides ? r : 0),
+        range_of(rel.attract.offsets, edge_bytes(rel.attract, r)),
+        range_of(rel.attract.ids, rel.attract.offsets ? rel.attract.edges * 4 : 0),
+        range_of(rel.repel.offsets, edge_bytes(rel.repel, r)),
+        range_of(rel.repel.ids, rel.repel.offsets ? rel.repel.edges * 4 : 0),
+        range_of(rel.ignore.offsets, edge_bytes(rel.ignore, r)),
+        range_of(rel.ignore.ids, rel.ignore.offsets ? rel.ignore.edges * 4 : 0),
+    };
+    const Range outputs[] = {
+        range_of(a->loss, 4),
+        range_of(a->d_scores, ((r - 1) * a->ld_d_scores + a->cols) * 4),
+        range_of(a->d_inverse_temperature, 4),
+        range_of(a->d_bias, 4),
+        range_of(a->workspace, wsb),
+        range_of(a->device_status, 4),
+    };
+    if (any_overlap(inputs, sizeof(inputs) / sizeof(inputs[0]), outputs, sizeof(outputs) / sizeof(outputs[0])))
+        return CLI_INVALID_ARGUMENT;
+    cudaStream_t stream = static_cast<cudaStream_t>(a->stream);
+    if (cudaMemsetAsync(a->device_status, 0, sizeof(int32_t), stream) != cudaSuccess) return CLI_DEVICE;
+    ScoreLossLaunch L;
+    L.rows = static_cast<int>(a->rows);
+    L.cols = static_cast<int>(a->cols);
+    L.ld = static_cast<long long>(a->ld);
+    L.ld_ds = static_cast<long long>(a->ld_d_scores);
+    L.scores = a->scores;
+    L.t_ptr = a->inverse_temperature;
+    L.b_ptr = a->bias;
+    L.sets[0] = to_set(rel.attract);
+    L.sets[1] = to_set(rel.repel);
+    L.sets[2] = to_set(rel.ignore);
+    L.named = rel.negatives_named ? 1 : 0;
+    L.ambient = rel.ambient_weight;
+    L.sides = a->sides;
+    L.loss = a->loss;
+    L.d_scores = a->d_scores;
+    L.dt = a->d_inverse_temperature;
+    L.db = a->d_bias;
+    L.partials = static_cast<float *>(a->workspace);
+    L.blocks = static_cast<int>(a->rows);
+    L.status = a->device_status;
+    if (launch_score_forms(f->form, L, stream) != cudaSuccess) return CLI_DEVICE;
+    return CLI_OK;
+}
+
 // ----------------------------------------------------------------------------
 // MaxSim
 // ----------------------------------------------------------------------------

@@ -83,6 +83,8 @@ struct ScoreLossLaunch {
     int32_t *status;
 };
 cudaError_t launch_score_loss(const ScoreLossLaunch &L, cudaStream_t stream);
+// balanced (form 1) and ranked (form 2); L.partials holds rows x 4 floats.
+cudaError_t launch_score_forms(int form, const ScoreLossLaunch &L, cudaStream_t stream);
 int score_loss_blocks(size_t rows, size_t cols);
 
 // MaxSim.

@@ -182,6 +182,38 @@ typedef struct {
 cli_status_t pair_loss_sigmoid_scores_fwd_bwd(const cli_pair_loss_sigmoid_scores_t *args);
 size_t pair_loss_sigmoid_scores_workspace_bytes(size_t rows, size_t cols);
 
+/* Pair-loss forms ("Training", `uform_pair_loss_form_t`; the values are the
+ * pages' enumerators). */
+typedef enum {
+    CLI_FORM_BALANCED = 1, /* the sigmoid cross-entropy of every cell, its attract and repel halves normalized apart */
+    CLI_FORM_RANKED = 2,   /* the sigmoid cross-entropy of every positive's score over every negative's; b cancels */
+    CLI_FORM_SIGMOID = 3   /* SigLIP's sigmoid cross-entropy of every cell, each repel weighed like an attract */
+} cli_pair_loss_form_t;
+
+/*
+ * pair_loss_scores_fwd_bwd -- a pair loss of the chosen form over a given
+ * rows x cols score matrix ("UForm", section "ColBERT-Style Late-Interaction
+ * Rerankers": each query's row of hard MaxSim scores is scored by the ranked
+ * form by default, and the balanced and SigLIP forms stay selectable).  The
+ * pages define balanced and ranked in words only; this library reads them as
+ *   balanced: l_p = sum_{attract} w l / sum_{attract} w + sum_{repel} w l / sum_{repel} w
+ *             with l the sigmoid form's cell loss, each half present only
+ *             when the row has such cells;
+ *   ranked:   l_p = sum_{i attract, j repel} w_i w_j softplus(-t (S_pi - S_pj))
+ *                   / (sum_i w_i sum_j w_j),  0 when either set is empty;
+ *   L = (1/rows) sum_p l_p.
+ * Cells are resolved exactly as in pair_loss_sigmoid_scores_fwd_bwd (relations,
+ * sides, negatives); form CLI_FORM_SIGMOID computes that verb's result.  db is
+ * 0 for the ranked form (the bias cancels).
+ */
+typedef struct {
+    int form;
+    cli_pair_loss_sigmoid_scores_t args;   /* every other field, as for the sigmoid form */
+} cli_pair_loss_scores_t;
+
+cli_status_t pair_loss_scores_fwd_bwd(const cli_pair_loss_scores_t *args);
+size_t pair_loss_scores_workspace_bytes(int form, size_t rows, size_t cols);
+
 /* A ragged tape of `count` items ("Arenas", "Rows and Tapes"): item k owns rows
  * offsets[k] .. offsets[k+1]-1 of `data`, which packs `rows` rows of `width`
  * bf16 values end to end.  `data` and `offsets` are device memory; `rows`
