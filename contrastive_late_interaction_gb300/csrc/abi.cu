@@ -167,6 +167,7 @@ cli_status_t pair_loss_sigmoid_fwd_bwd(const cli_pair_loss_sigmoid_t *a) {
     L.d_e = a->d_embeddings;
     L.ld_de = static_cast<long long>(a->ld_d_embeddings);
     L.partials = ws.partials;
+    L.sums = ws.sums;
     L.loss = a->loss;
     L.dt = a->d_inverse_temperature;
     L.db = a->d_bias;

@@ -37,7 +37,8 @@ struct PooledWorkspace {
     uint32_t *rel_cnt;     // [n]
     uint32_t *rel_off;     // [n+1]
     RelEntry *rel;         // [2 E_total + n]
-    float *partials;       // [tile_pairs][4][4]
+    float *partials;       // [pooled_partial_slots(n)][4]
+    double *sums;          // [pooled_finish_blocks()][3]
     size_t bytes;
 };
 
@@ -54,6 +55,7 @@ struct PooledLaunch {
     float *d_e;
     long long ld_de;
     float *partials;
+    double *sums;
     float *loss, *dt, *db;
     int32_t *status;
     int sm_count;
@@ -65,7 +67,8 @@ cudaError_t launch_relation_prep(const EdgeSet sets[3], int n, int named, float 
 
 cudaError_t launch_pooled_fused(const CUtensorMap &tmap_e, const PooledLaunch &L, cudaStream_t stream);
 size_t pooled_fused_smem_bytes();
-long long pooled_tile_pairs(int n);
+long long pooled_partial_slots(int n);
+int pooled_finish_blocks();
 
 // Score-matrix loss.
 struct ScoreLossLaunch {

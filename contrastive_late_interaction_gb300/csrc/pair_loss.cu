@@ -1,4 +1,5 @@
-// Pooled sigmoid pair loss, forward and backward, fused over 128 x 128 tiles.
+// Pooled sigmoid pair loss, forward and backward, fused over 256 x 256 blocks
+// of the score matrix.
 //
 // What is computed ("UForm", section "Matryoshka-Like Multi-Scale Embedders",
 // the SigLIP loss; "Training", `uform_pair_loss_form_t` = sigmoid,
@@ -7,29 +8,35 @@
 //     L = (1/N) sum_{i != j} l_ij,  dE, dt, db.
 //
 // GB300 design.  The score matrix is symmetric (s_ij = s_ji) and, with one
-// temperature group, so is z.  The kernel therefore visits only tile pairs
-// (I, J) with I <= J.  For each one:
-//   1. tcgen05 computes S_IJ = E_I E_J^T into TMEM (bf16 operands staged by TMA
-//      in 128-byte-swizzled 128 x 64 boxes, fp32 accumulation);
-//   2. four epilogue warps read S_IJ from TMEM, one row per thread, and for
-//      every cell evaluate one sigmoid and one softplus that serve both ordered
-//      pairs (i, j) and (j, i): p = sigma(z), sp = softplus(z).  With each
-//      direction's resolved (attract?, weight) the gradient of the two pairs
-//      is G_ij = sum_dir w (p - [attract]) and the loss w (sp - [attract] z).
-//      H_IJ = (t/N) G_IJ is written as bf16 into shared memory; partial sums
-//      of the loss, G*s (for dt) and G (for db) go to a fixed slot per warp;
-//   3. tcgen05 computes the two gradient contractions from shared memory,
-//      dE_I += H_IJ E_J and (I != J) dE_J += H_IJ^T E_I, in 64-column chunks,
-//      reading H and the E tiles in both K-major and MN-major form from the
-//      same bytes; the epilogue warps add each chunk into dE (fp32) with
-//      vector reductions.
-// Neither S nor H ever reaches device memory.  Relations are resolved once
-// per call into a per-row sorted list of "special" columns (both directions
-// of every pair some edge set names, plus the diagonal); every other cell
-// takes the run's default.
-//
-// Two CTAs share an SM (about 97 KB of shared memory and 256 TMEM columns
-// each), so one CTA's epilogue overlaps the other's tensor-core work.
+// temperature group, so is z.  The kernel visits the upper triangle of 2 x 2
+// blocks of 128 x 128 tiles: rows I0, I1 = I0 + 1 against columns J0, J1 =
+// J0 + 1 (on a diagonal block the columns are the rows, and the mirrored tile
+// (I1, I0) is skipped).  One persistent CTA per SM; for each block:
+//   1. S pass.  tcgen05 computes the four tiles S_xy = E_Ix E_Jy^T into the
+//      512 TMEM columns (bf16 operands staged by TMA in 128-byte-swizzled
+//      128 x 64 boxes, fp32 accumulation).  The four boxes of one K step fill
+//      a stage; the shared memory that holds H later is lent to the pass as
+//      two more stages.
+//   2. Epilogue.  Eight warps read S from TMEM, one row per thread (two warps
+//      per TMEM lane quarter, one per tile row), and for every cell evaluate
+//      one sigmoid and one softplus that serve both ordered pairs (i, j) and
+//      (j, i): with each direction's resolved (attract?, weight) the gradient
+//      of the two pairs is G_ij = sum_dir w (p - [attract]) and the loss
+//      w (sp - [attract] z).  H_xy = (t/N) G_xy goes to shared memory as bf16;
+//      partial sums of the loss, G*s (for dt) and G (for db) go to a fixed
+//      slot per warp.
+//   3. Gradient pass.  Per 64 columns of D, tcgen05 accumulates
+//          dE_Ix += sum_y H_xy E_Jy,   dE_Jy += sum_x H_xy^T E_Ix
+//      in four TMEM accumulators (two on a diagonal block, where the rows and
+//      columns coincide), reading H and the E boxes in both K-major and
+//      MN-major form from the same bytes; the epilogue warps add each chunk
+//      into dE (fp32) with vector reductions while the next chunk's MMAs run.
+// Each accumulator sums the contributions of two tiles before it leaves the
+// SM, so per FLOP half as many fp32 partials reach L2 as with single tile
+// pairs: L2 reductions of dE are what bound this kernel.  Neither S nor H ever
+// reaches device memory.  Relations are resolved once per call into a per-row
+// sorted list of "special" columns (both directions of every pair some edge
+// set names, plus the diagonal); every other cell takes the run's default.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -43,27 +50,30 @@ namespace pooled {
 
 constexpr int BM = 128;                 // tile rows and columns
 constexpr int BK = 64;                  // K extent of one TMA box (128 bytes of bf16)
-constexpr int STAGES = 2;
 constexpr uint32_t BOX_BYTES = BM * BK * 2;   // 16 KB
-constexpr int kThreads = 192;           // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
-constexpr uint32_t TMEM_COLS = 256;
-constexpr uint32_t TM_S = 0, TM_DEI = 128, TM_DEJ = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2..9 epilogue
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int kStages = 3;              // stage 0: the box ring; stages 1, 2: the H region, lent to the S pass
+constexpr int kPartialsPerBlock = kEpiWarps;
+constexpr int kFinishBlocks = 256;
 
 struct SharedStorage {
-    alignas(1024) uint8_t ring[STAGES][2][BOX_BYTES];
-    alignas(1024) uint8_t h[2][BOX_BYTES];     // H tile, two 64-column K blocks
-    alignas(16) float stage_t[4][32 * 16];     // per epilogue warp: 32 rows x 16 fp32, transposed drain
-    uint64_t full[STAGES], empty[STAGES];
-    uint64_t s_full, s_free, h_ready, h_free, de_full, de_free, mma_done;
+    alignas(1024) uint8_t ring[4][BOX_BYTES];   // stage 0: boxes of I0, I1, J0, J1
+    alignas(1024) uint8_t hreg[8][BOX_BYTES];   // H tiles 0..3 (two boxes each); stages 1 and 2 of the S pass
+    alignas(16) float stage_t[kEpiWarps][32 * 16];   // per epilogue warp: 32 rows x 16 fp32, transposed drain
+    uint64_t full[kStages], empty[kStages];
+    uint64_t s_full, h_ready, h_free, de_full[2], de_free[2], mma_done;
     uint32_t tmem_base;
     int abort_flag;
 };
 
 constexpr size_t kSmemBytes = sizeof(SharedStorage) + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 struct Params {
-    int n, width, nk, nb;
-    long long tile_pairs;
+    int n, width, nk, nb, nbb;
+    long long blocks;
     const float *t_ptr, *b_ptr;
     float ambient;
     int named;
@@ -71,16 +81,16 @@ struct Params {
     const RelEntry *rel;
     float *d_e;
     long long ld_de;
-    float *partials;   // [tile_pairs][4 warps][4]
+    float *partials;   // [blocks][kEpiWarps][4]
     int32_t *status;
 };
 
-// Tile pair p -> (I, J), I <= J.  The upper triangle of tile pairs is walked in
-// super-blocks of kSuper x kSuper tiles (row-major over super-blocks I' <= J',
+// Pair p -> (I, J), I <= J, over an n x n grid.  The upper triangle is walked
+// in super-blocks of kSuper x kSuper (row-major over super-blocks I' <= J',
 // then row-major inside a super-block, keeping I <= J on the diagonal ones),
 // so the CTAs running at the same time read and reduce into the rows of a few
 // super-blocks only: their E rows and dE rows stay resident in L2.
-constexpr int kSuper = 8;
+constexpr int kSuper = 4;
 
 // Row-major enumeration of the upper triangle of an n x n grid: index -> (i, j).
 __device__ __forceinline__ void tri_decode(long long p, int n, int &i, int &j) {
@@ -98,12 +108,10 @@ __device__ __forceinline__ void tri_decode(long long p, int n, int &i, int &j) {
 
 __device__ __forceinline__ void decode_pair(long long p, int nb, int &I, int &J) {
     const int ns = (nb + kSuper - 1) / kSuper;          // super-blocks per side
-    const int last = nb - (ns - 1) * kSuper;            // tiles in the last super-block row/column
-    // walk super-blocks (si, sj), si <= sj, counting the tile pairs each holds
+    const int last = nb - (ns - 1) * kSuper;            // entries in the last super-block row/column
     long long before = 0;
     for (int si = 0; si < ns; ++si) {
         const int hi = si == ns - 1 ? last : kSuper;
-        // off-diagonal super-blocks of this row: (ns - 1 - si) of them, the last one narrower
         const long long diag = static_cast<long long>(hi) * (hi + 1) / 2;
         const long long full_off = si < ns - 1 ? static_cast<long long>(ns - 2 - si) * hi * kSuper + static_cast<long long>(hi) * last : 0;
         if (p < before + diag + full_off) {
@@ -116,7 +124,6 @@ __device__ __forceinline__ void decode_pair(long long p, int nb, int &I, int &J)
                 return;
             }
             q -= diag;
-            // off-diagonal super-blocks sj = si+1 .. ns-1, each hi x width(sj), row-major
             for (int sj = si + 1; sj < ns; ++sj) {
                 const int w = sj == ns - 1 ? last : kSuper;
                 const long long cnt = static_cast<long long>(hi) * w;
@@ -130,8 +137,37 @@ __device__ __forceinline__ void decode_pair(long long p, int nb, int &I, int &J)
         }
         before += diag + full_off;
     }
-    I = J = nb - 1;   // not reached for p < tile_pairs
+    I = J = nb - 1;   // not reached for p < nb (nb + 1) / 2
 }
+
+// One 2 x 2 block of tiles.  Slot (x, y) is the tile pair (I0 + x, J0 + y);
+// box position 0..3 holds the E rows of I0, I1, J0, J1; accumulator 0..3
+// collects dE of the same four tile rows (on a diagonal block J = I, so the
+// column side lands in accumulators 0 and 1 and positions 2, 3 are unused).
+struct Block {
+    int I0, J0;
+    bool diag, i1, j1;
+};
+
+__device__ __forceinline__ Block decode_block(long long p, const Params &P) {
+    int bi, bj;
+    decode_pair(p, P.nbb, bi, bj);
+    Block b;
+    b.I0 = 2 * bi;
+    b.J0 = 2 * bj;
+    b.diag = bi == bj;
+    b.i1 = b.I0 + 1 < P.nb;
+    b.j1 = b.J0 + 1 < P.nb;
+    return b;
+}
+__device__ __forceinline__ bool slot_on(const Block &b, int x, int y) {
+    return (x == 0 || b.i1) && (y == 0 || b.j1) && !(b.diag && x == 1 && y == 0);
+}
+__device__ __forceinline__ bool box_on(const Block &b, int pos) {
+    return pos == 0 || (pos == 1 ? b.i1 : (!b.diag && (pos == 2 || b.j1)));
+}
+__device__ __forceinline__ int col_pos(const Block &b, int y) { return b.diag ? y : 2 + y; }
+__device__ __forceinline__ int box_tile(const Block &b, int pos) { return pos < 2 ? b.I0 + pos : b.J0 + pos - 2; }
 
 __device__ __forceinline__ float fast_ex2(float x) {
     float y;
@@ -156,8 +192,8 @@ __device__ __forceinline__ float fast_rcp(float x) {
 struct CellFn {
     float p, pc, sp;
 };
+constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
 __device__ __forceinline__ CellFn cell_fn(float z) {
-    const float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
     float e = fast_ex2(-fabsf(z) * kLog2e);
     float q = 1.0f + e;
     float r = fast_rcp(q);
@@ -170,14 +206,46 @@ __device__ __forceinline__ CellFn cell_fn(float z) {
     c.sp = fmaxf(z, 0.0f) + l1p;
     return c;
 }
+// The same where |z| >= kFarZ, so e < 2^-7: 1/(1+e) = 1 - e + e^2 with
+// relative error below e^3 < 2^-21, and log1p(e) = e(1 - e/2).  One MUFU op.
+constexpr float kFarZ = 4.86f;   // > 7 ln 2
+__device__ __forceinline__ CellFn cell_fn_far(float z) {
+    const float e = fast_ex2(-fabsf(z) * kLog2e);
+    const float r = fmaf(e, e - 1.0f, 1.0f);
+    const float er = e * r;
+    const bool pos = z >= 0.0f;
+    CellFn c;
+    c.p = pos ? r : er;
+    c.pc = pos ? er : r;
+    c.sp = fmaxf(z, 0.0f) + fmaf(-0.5f * e, e, e);
+    return c;
+}
 
 __device__ __forceinline__ void red_add_v4(float *gptr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gptr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
-    fused_tiles_kernel(const __grid_constant__ CUtensorMap tmap_e, Params P) {
+// Default cells of one 32-column chunk: accumulate the sums and write H.
+template <bool kFar>
+__device__ __forceinline__ void default_cells(const float (&v)[32], float t, float b, bool row_ok, int valid,
+                                              float hscale, float &acc_sp, float &acc_p, float &acc_ps,
+                                              float (&hv)[32]) {
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+        const float s = v[r];
+        const float z = fmaf(t, s, b);
+        const CellFn f = kFar ? cell_fn_far(z) : cell_fn(z);
+        const bool ok_col = row_ok && r < valid;
+        acc_sp += ok_col ? f.sp : 0.f;
+        acc_p += ok_col ? f.p : 0.f;
+        acc_ps += ok_col ? f.p * s : 0.f;
+        hv[r] = ok_col ? hscale * f.p : 0.f;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fused_blocks_kernel(const __grid_constant__ CUtensorMap tmap_e, Params P) {
     extern __shared__ uint8_t smem_raw[];
     SharedStorage &sm = *reinterpret_cast<SharedStorage *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -186,16 +254,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (read_status(P.status) != 0) return;  // an earlier stage of the call failed
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1);
         }
         mbar_init(&sm.s_full, 1);
-        mbar_init(&sm.s_free, 4);
-        mbar_init(&sm.h_ready, 4);
+        mbar_init(&sm.h_ready, kEpiWarps);
         mbar_init(&sm.h_free, 1);
-        mbar_init(&sm.de_full, 1);
-        mbar_init(&sm.de_free, 4);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.de_full[b], 1);
+            mbar_init(&sm.de_free[b], kEpiWarps);
+        }
         mbar_init(&sm.mma_done, 1);
         sm.abort_flag = 0;
         fence_mbar_init();
@@ -207,92 +276,114 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     volatile int *abort_flag = &sm.abort_flag;
+    // Box `pos` of stage `s`: stage 0 is the ring, stages 1 and 2 the two halves of the H region.
+    auto box_ptr = [&](int s, int pos) -> uint8_t * { return s == 0 ? sm.ring[pos] : sm.hreg[(s - 1) * 4 + pos]; };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
+            uint32_t ph = 0;   // bit s: parity of stage s's next use
+            uint32_t kblk = 0;
             bool ok = true;
-            for (long long p = blockIdx.x; p < P.tile_pairs && ok; p += gridDim.x) {
-                int I, J;
-                decode_pair(p, P.nb, I, J);
-                const bool diag = I == J;
-                for (int pass = 0; pass < 2 && ok; ++pass) {   // S pass, then the dE pass
+            for (long long p = blockIdx.x; p < P.blocks && ok; p += gridDim.x, ++kblk) {
+                const Block bk = decode_block(p, P);
+                int nbox = 0;
+                for (int pos = 0; pos < 4; ++pos) nbox += box_on(bk, pos) ? 1 : 0;
+                bool h_owned = false;
+                for (int pass = 0; pass < 2 && ok; ++pass) {   // S pass, then the gradient pass
                     for (int kc = 0; kc < P.nk; ++kc) {
-                        if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag, P.status, kSleepProducer)) { ok = false; break; }
-                        mbar_arrive_expect_tx(&sm.full[stage], diag ? BOX_BYTES : 2 * BOX_BYTES);
-                        tma_load_2d(sm.ring[stage][0], &tmap_e, &sm.full[stage], kc * BK, I * BM);
-                        if (!diag) tma_load_2d(sm.ring[stage][1], &tmap_e, &sm.full[stage], kc * BK, J * BM);
-                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                        const int s = pass == 0 ? kc % kStages : 0;
+                        if (s != 0 && !h_owned) {
+                            // The H region holds the previous block's H until its gradient MMAs are done.
+                            if (!mbar_wait(&sm.h_free, (kblk & 1) ^ 1, abort_flag, P.status, kSleepProducer)) { ok = false; break; }
+                            h_owned = true;
+                        }
+                        if (!mbar_wait(&sm.empty[s], ((ph >> s) & 1) ^ 1, abort_flag, P.status, kSleepProducer)) { ok = false; break; }
+                        mbar_arrive_expect_tx(&sm.full[s], nbox * BOX_BYTES);
+                        for (int pos = 0; pos < 4; ++pos)
+                            if (box_on(bk, pos))
+                                tma_load_2d(box_ptr(s, pos), &tmap_e, &sm.full[s], kc * BK, box_tile(bk, pos) * BM);
+                        ph ^= 1u << s;
                     }
                 }
             }
             // Let in-flight loads land before the CTA can exit.
-            for (int s = 0; s < STAGES; ++s) mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag, P.status),
-                                              (++stage == STAGES ? (stage = 0, phase ^= 1) : 0);
+            for (int s = 0; s < kStages; ++s) mbar_wait(&sm.empty[s], ((ph >> s) & 1) ^ 1, abort_flag, P.status);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
-            const uint32_t idesc_di = idesc_bf16(128, 64, 0, 1);   // A = H (K-major), B = E_J (MN-major)
-            const uint32_t idesc_dj = idesc_bf16(128, 64, 1, 1);   // A = H^T (MN-major), B = E_I (MN-major)
-            const uint32_t h0 = smem_u32(sm.h[0]);
-            int stage = 0;
-            uint32_t phase = 0, k = 0, chunk = 0;
+            const uint32_t idesc_row = idesc_bf16(128, 64, 0, 1);   // A = H (K-major), B = E_J (MN-major)
+            const uint32_t idesc_col = idesc_bf16(128, 64, 1, 1);   // A = H^T (MN-major), B = E_I (MN-major)
+            uint32_t ph = 0;   // bit s: parity of stage s's next use
+            uint32_t kblk = 0, chunk = 0;
             bool ok = true;
-            for (long long p = blockIdx.x; p < P.tile_pairs && ok; p += gridDim.x, ++k) {
-                int I, J;
-                decode_pair(p, P.nb, I, J);
-                const bool diag = I == J;
-                // S = E_I E_J^T
-                if (!mbar_wait(&sm.s_free, (k & 1) ^ 1, abort_flag, P.status, kSleepIssuer)) break;
+            for (long long p = blockIdx.x; p < P.blocks && ok; p += gridDim.x, ++kblk) {
+                const Block bk = decode_block(p, P);
+                // S takes every TMEM column: wait until the last gradient chunk has been drained.
+                if (chunk > 0 && !mbar_wait(&sm.de_free[(chunk - 1) & 1], ((chunk - 1) >> 1) & 1, abort_flag, P.status,
+                                            kSleepIssuer))
+                    break;
                 tc_fence_after();
                 for (int kc = 0; kc < P.nk; ++kc) {
-                    if (!mbar_wait(&sm.full[stage], phase, abort_flag, P.status, kSleepIssuer)) { ok = false; break; }
+                    const int s = kc % kStages;
+                    if (!mbar_wait(&sm.full[s], (ph >> s) & 1, abort_flag, P.status, kSleepIssuer)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a = smem_u32(sm.ring[stage][0]);
-                    const uint32_t b = diag ? a : smem_u32(sm.ring[stage][1]);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_bf16(tmem + TM_S, sdesc_sw128(a + kk * 32, 16, 1024), sdesc_sw128(b + kk * 32, 16, 1024),
-                                 idesc_s, (kc | kk) != 0);
-                    mma_commit(&sm.empty[stage]);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    for (int x = 0; x < 2; ++x)
+#pragma unroll
+                        for (int y = 0; y < 2; ++y) {
+                            if (!slot_on(bk, x, y)) continue;
+                            const uint32_t a = smem_u32(box_ptr(s, x)), b = smem_u32(box_ptr(s, col_pos(bk, y)));
+#pragma unroll
+                            for (int kk = 0; kk < BK / 16; ++kk)
+                                mma_bf16(tmem + (2 * x + y) * BM, sdesc_sw128(a + kk * 32, 16, 1024),
+                                         sdesc_sw128(b + kk * 32, 16, 1024), idesc_s, (kc | kk) != 0);
+                        }
+                    mma_commit(&sm.empty[s]);
+                    ph ^= 1u << s;
                 }
                 if (!ok) break;
                 mma_commit(&sm.s_full);
-                // dE_I += H E_J, dE_J += H^T E_I, 64 columns of D at a time
-                if (!mbar_wait(&sm.h_ready, k & 1, abort_flag, P.status, kSleepIssuer)) break;
+                // Gradient pass, 64 columns of D at a time, into TMEM buffer (chunk & 1).
+                if (!mbar_wait(&sm.h_ready, kblk & 1, abort_flag, P.status, kSleepIssuer)) break;
                 tc_fence_after();
                 for (int dc = 0; dc < P.nk; ++dc, ++chunk) {
-                    if (!mbar_wait(&sm.full[stage], phase, abort_flag, P.status, kSleepIssuer)) { ok = false; break; }
-                    if (!mbar_wait(&sm.de_free, (chunk & 1) ^ 1, abort_flag, P.status, kSleepIssuer)) { ok = false; break; }
+                    const uint32_t buf = chunk & 1;
+                    if (!mbar_wait(&sm.full[0], ph & 1, abort_flag, P.status, kSleepIssuer)) { ok = false; break; }
+                    if (!mbar_wait(&sm.de_free[buf], ((chunk >> 1) & 1) ^ 1, abort_flag, P.status, kSleepIssuer)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t ei = smem_u32(sm.ring[stage][0]);
-                    const uint32_t ej = diag ? ei : smem_u32(sm.ring[stage][1]);
+                    const uint32_t acc0 = tmem + buf * 256;
+                    uint32_t started = 0;   // bit a: accumulator a holds this chunk's first product
 #pragma unroll
-                    for (int kk = 0; kk < BM / 16; ++kk) {
-                        // A: H rows i, K = j (16 per step) inside 64-wide K blocks.
-                        const uint64_t a = sdesc_sw128(h0 + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
-                        // B: E_J box viewed as [N = 64 features] x [K = j]; 16 rows of j = 2048 bytes.
-                        const uint64_t b = sdesc_sw128(ej + kk * 2048, 1024, 1024);
-                        mma_bf16(tmem + TM_DEI, a, b, idesc_di, kk != 0);
-                    }
-                    if (!diag) {
+                    for (int x = 0; x < 2; ++x)
 #pragma unroll
-                        for (int kk = 0; kk < BM / 16; ++kk) {
-                            // A: H viewed as [M = j] x [K = i]: j contiguous within a 64-wide block
-                            // (blocks BOX_BYTES apart), 8 rows of i per 1024 bytes.
-                            const uint64_t a = sdesc_sw128(h0 + kk * 2048, BOX_BYTES, 1024);
-                            const uint64_t b = sdesc_sw128(ei + kk * 2048, 1024, 1024);
-                            mma_bf16(tmem + TM_DEJ, a, b, idesc_dj, kk != 0);
+                        for (int y = 0; y < 2; ++y) {
+                            if (!slot_on(bk, x, y)) continue;
+                            const uint32_t h = smem_u32(sm.hreg[2 * (2 * x + y)]);
+                            // Row side: acc[x] += H_xy E_Jy.  A: H rows i, K = j (16 per step) inside
+                            // 64-wide K blocks; B: the E_Jy box viewed as [N = 64 features] x [K = j].
+                            const uint32_t ej = smem_u32(box_ptr(0, col_pos(bk, y)));
+#pragma unroll
+                            for (int kk = 0; kk < BM / 16; ++kk)
+                                mma_bf16(acc0 + x * 64, sdesc_sw128(h + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024),
+                                         sdesc_sw128(ej + kk * 2048, 1024, 1024), idesc_row, ((started >> x) & 1) || kk != 0);
+                            started |= 1u << x;
+                            if (bk.diag && x == y) continue;   // a diagonal tile: H is symmetric, the row side is all
+                            // Column side: acc[col] += H_xy^T E_Ix.  A: H viewed as [M = j] x [K = i], j
+                            // contiguous within a 64-wide block (blocks BOX_BYTES apart), 8 rows of i per 1024 bytes.
+                            const int ca = col_pos(bk, y);
+                            const uint32_t ei = smem_u32(box_ptr(0, x));
+#pragma unroll
+                            for (int kk = 0; kk < BM / 16; ++kk)
+                                mma_bf16(acc0 + ca * 64, sdesc_sw128(h + kk * 2048, BOX_BYTES, 1024),
+                                         sdesc_sw128(ei + kk * 2048, 1024, 1024), idesc_col, ((started >> ca) & 1) || kk != 0);
+                            started |= 1u << ca;
                         }
-                    }
-                    mma_commit(&sm.empty[stage]);
-                    mma_commit(&sm.de_full);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    mma_commit(&sm.empty[0]);
+                    ph ^= 1u;
+                    mma_commit(&sm.de_full[buf]);
                 }
                 if (!ok) break;
                 mma_commit(&sm.h_free);
@@ -302,101 +393,102 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     } else {
         // ------------------------------------------------------------ epilogue warps
+        const int ew = warp - 2;                 // 0..7
         const int quad = warp & 3;               // TMEM lane quadrant this warp may access
+        const int x = ew >> 2;                   // tile row of the block this warp reads (and drains)
         const int row = quad * 32 + lane;        // row of the tile this thread owns
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const float t = *P.t_ptr, b = *P.b_ptr;
         const float inv_n = 1.0f / static_cast<float>(P.n);
         const float c_h = t * inv_n;             // H = (t/N) G
         const float w_d = P.named ? 0.0f : P.ambient;
-        const uint32_t h0 = smem_u32(sm.h[0]);
-        const uint32_t stage_s = smem_u32(sm.stage_t[quad]);
-        uint32_t k = 0, chunk = 0;
-        for (long long p = blockIdx.x; p < P.tile_pairs; p += gridDim.x, ++k) {
-            int I, J;
-            decode_pair(p, P.nb, I, J);
-            const bool diag = I == J;
-            const int gi = I * BM + row;          // this thread's item (anchor)
-            const bool row_ok = gi < P.n;
-            const int j0 = J * BM;
-            // This row's special columns inside [j0, j0 + 128).
-            uint32_t e_beg = 0, e_end = 0;
+        const uint32_t stage_s = smem_u32(sm.stage_t[ew]);
+        uint32_t kblk = 0, chunk = 0;
+        for (long long p = blockIdx.x; p < P.blocks; p += gridDim.x, ++kblk) {
+            const Block bk = decode_block(p, P);
+            const bool x_on = x == 0 || bk.i1;
+            const int gi = (bk.I0 + x) * BM + row;   // this thread's item (anchor)
+            const bool row_ok = x_on && gi < P.n;
+            const int y_first = (bk.diag && x == 1) ? 1 : 0;
+            // This row's special columns from the first tile column it reads on.
+            uint32_t e = 0, e_end = 0;
             if (row_ok) {
+                const uint32_t jfirst = static_cast<uint32_t>((bk.J0 + y_first) * BM);
                 uint32_t lo = P.rel_off[gi], hi = P.rel_off[gi + 1];
                 e_end = hi;
                 while (lo < hi) {
-                    uint32_t mid = (lo + hi) >> 1;
-                    if (P.rel[mid].col < static_cast<uint32_t>(j0)) lo = mid + 1; else hi = mid;
+                    const uint32_t mid = (lo + hi) >> 1;
+                    if (P.rel[mid].col < jfirst) lo = mid + 1; else hi = mid;
                 }
-                e_beg = lo;
+                e = lo;
             }
-            if (!mbar_wait(&sm.s_full, k & 1, abort_flag, P.status, kSleepEpilogue)) break;
-            if (!mbar_wait(&sm.h_free, (k & 1) ^ 1, abort_flag, P.status, kSleepEpilogue)) break;
+            if (!mbar_wait(&sm.s_full, kblk & 1, abort_flag, P.status, kSleepEpilogue)) break;
             tc_fence_after();
 
-            float acc_sp = 0.f, acc_p = 0.f, acc_ps = 0.f;     // default cells (times 2 w_d later)
-            float fix_l = 0.f, fix_g = 0.f, fix_gs = 0.f;     // corrections for special cells
-            uint32_t e = e_beg;
+            float l_sum = 0.f, g_sum = 0.f, gs_sum = 0.f;
+            for (int y = y_first; y < 2; ++y) {
+                if (!slot_on(bk, x, y)) continue;   // warp-uniform
+                const int slot = 2 * x + y;
+                const int j0 = (bk.J0 + y) * BM;
+                const uint32_t hbase = smem_u32(sm.hreg[2 * slot]);
+                float acc_sp = 0.f, acc_p = 0.f, acc_ps = 0.f;   // default cells (times 2 w_d later)
+                float fix_l = 0.f, fix_g = 0.f, fix_gs = 0.f;   // corrections for special cells
 #pragma unroll 1
-            for (int ch = 0; ch < BM / 32; ++ch) {
-                float v[32];
-                tmem_ld32(tmem + lane_base + TM_S + ch * 32, v);
-                const int c0 = j0 + ch * 32;
-                const int valid = min(32, P.n - c0);     // columns of this chunk inside the batch
-                float hv[32];
+                for (int ch = 0; ch < BM / 32; ++ch) {
+                    float v[32];
+                    tmem_ld32(tmem + lane_base + slot * BM + ch * 32, v);
+                    const int c0 = j0 + ch * 32;
+                    const int valid = min(32, P.n - c0);   // columns of this chunk inside the batch
+                    float zmin = 3.0e38f;
 #pragma unroll
-                for (int r = 0; r < 32; ++r) {
-                    const float s = v[r];
-                    const float z = fmaf(t, s, b);
-                    const CellFn f = cell_fn(z);
-                    const bool ok_col = row_ok && r < valid;
-                    acc_sp += ok_col ? f.sp : 0.f;
-                    acc_p += ok_col ? f.p : 0.f;
-                    acc_ps += ok_col ? f.p * s : 0.f;
-                    hv[r] = ok_col ? c_h * 2.0f * w_d * f.p : 0.f;
+                    for (int r = 0; r < 32; ++r) zmin = fminf(zmin, fabsf(fmaf(t, v[r], b)));
+                    float hv[32];
+                    const float hscale = c_h * 2.0f * w_d;
+                    if (__all_sync(0xffffffffu, zmin >= kFarZ))
+                        default_cells<true>(v, t, b, row_ok, valid, hscale, acc_sp, acc_p, acc_ps, hv);
+                    else
+                        default_cells<false>(v, t, b, row_ok, valid, hscale, acc_sp, acc_p, acc_ps, hv);
+                    // Special cells: replace the default by the resolved pair of directions.
+                    while (e < e_end) {
+                        const RelEntry en = P.rel[e];
+                        if (en.col >= static_cast<uint32_t>(c0 + 32)) break;
+                        ++e;
+                        const int r = static_cast<int>(en.col) - c0;
+                        float s = 0.f;
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) s = (q == r) ? v[q] : s;
+                        const float z = fmaf(t, s, b);
+                        const CellFn f = cell_fn(z);
+                        const bool ao = en.flags & 1u, ai = en.flags & 2u;
+                        const float g = en.w_out * (ao ? -f.pc : f.p) + en.w_in * (ai ? -f.pc : f.p);
+                        const float l = en.w_out * (ao ? f.sp - z : f.sp) + en.w_in * (ai ? f.sp - z : f.sp);
+                        const float g_def = 2.0f * w_d * f.p;
+                        fix_l += l - 2.0f * w_d * f.sp;
+                        fix_g += g - g_def;
+                        fix_gs += (g - g_def) * s;
+                        const float hnew = c_h * g;
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) hv[q] = (q == r) ? hnew : hv[q];
+                    }
+                    // bf16 H row segment into the swizzled K-major tile.
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t col = ch * 32 + q * 8;
+                        st_shared_v4(hbase + sw128_bf16_offset(row, col, BM), pack_bf16x2(hv[q * 8 + 0], hv[q * 8 + 1]),
+                                     pack_bf16x2(hv[q * 8 + 2], hv[q * 8 + 3]), pack_bf16x2(hv[q * 8 + 4], hv[q * 8 + 5]),
+                                     pack_bf16x2(hv[q * 8 + 6], hv[q * 8 + 7]));
+                    }
                 }
-                // Special cells: replace the default by the resolved pair of directions.
-                while (e < e_end) {
-                    const RelEntry en = P.rel[e];
-                    if (en.col >= static_cast<uint32_t>(c0 + 32)) break;
-                    ++e;
-                    const int r = static_cast<int>(en.col) - c0;
-                    float s = 0.f;
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) s = (q == r) ? v[q] : s;
-                    const float z = fmaf(t, s, b);
-                    const CellFn f = cell_fn(z);
-                    const bool ao = en.flags & 1u, ai = en.flags & 2u;
-                    const float g = en.w_out * (ao ? -f.pc : f.p) + en.w_in * (ai ? -f.pc : f.p);
-                    const float l = en.w_out * (ao ? f.sp - z : f.sp) + en.w_in * (ai ? f.sp - z : f.sp);
-                    const float g_def = 2.0f * w_d * f.p;
-                    fix_l += l - 2.0f * w_d * f.sp;
-                    fix_g += g - g_def;
-                    fix_gs += (g - g_def) * s;
-                    const float hnew = c_h * g;
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) hv[q] = (q == r) ? hnew : hv[q];
-                }
-                // bf16 H row segment into the swizzled K-major tile.
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t col = ch * 32 + q * 8;
-                    st_shared_v4(h0 + sw128_bf16_offset(row, col, BM), pack_bf16x2(hv[q * 8 + 0], hv[q * 8 + 1]),
-                                 pack_bf16x2(hv[q * 8 + 2], hv[q * 8 + 3]), pack_bf16x2(hv[q * 8 + 4], hv[q * 8 + 5]),
-                                 pack_bf16x2(hv[q * 8 + 6], hv[q * 8 + 7]));
-                }
+                // A diagonal tile sees every unordered pair twice.
+                const float scale = (bk.diag && x == y) ? 0.5f : 1.0f;
+                l_sum += scale * (2.0f * w_d * acc_sp + fix_l);
+                g_sum += scale * (2.0f * w_d * acc_p + fix_g);
+                gs_sum += scale * (2.0f * w_d * acc_ps + fix_gs);
             }
             tc_fence_before();
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&sm.s_free);
-                mbar_arrive(&sm.h_ready);
-            }
-            // Per-warp partial sums of this tile pair (diagonal tiles see every pair twice).
-            float l_sum = 2.0f * w_d * acc_sp + fix_l;
-            float g_sum = 2.0f * w_d * acc_p + fix_g;
-            float gs_sum = 2.0f * w_d * acc_ps + fix_gs;
+            if (lane == 0) mbar_arrive(&sm.h_ready);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 l_sum += __shfl_xor_sync(0xffffffffu, l_sum, o);
@@ -404,25 +496,26 @@ __global__ void __launch_bounds__(kThreads, 2)
                 gs_sum += __shfl_xor_sync(0xffffffffu, gs_sum, o);
             }
             if (lane == 0) {
-                const float scale = diag ? 0.5f : 1.0f;
-                float *slot = P.partials + (p * 4 + quad) * 4;
-                slot[0] = l_sum * scale;
-                slot[1] = gs_sum * scale;
-                slot[2] = g_sum * scale;
+                float *slot = P.partials + (p * kPartialsPerBlock + ew) * 4;
+                slot[0] = l_sum;
+                slot[1] = gs_sum;
+                slot[2] = g_sum;
                 slot[3] = 0.f;
             }
-            // Drain the gradient chunks into dE.
+            // Drain the gradient chunks into dE: this warp takes accumulators x and 2 + x.
             bool ok = true;
             for (int dc = 0; dc < P.nk; ++dc, ++chunk) {
-                if (!mbar_wait(&sm.de_full, chunk & 1, abort_flag, P.status, kSleepEpilogue)) { ok = false; break; }
+                const uint32_t buf = chunk & 1;
+                if (!mbar_wait(&sm.de_full[buf], (chunk >> 1) & 1, abort_flag, P.status, kSleepEpilogue)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll 1
-                for (int side = 0; side < (diag ? 1 : 2); ++side) {
-                    const int row0 = (side == 0 ? I : J) * BM + quad * 32;   // first row of this warp's 32
+                for (int a = x; a < 4; a += 2) {
+                    if (!box_on(bk, a)) continue;   // warp-uniform: the accumulator of an absent tile row
+                    const int row0 = box_tile(bk, a) * BM + quad * 32;   // first row of this warp's 32
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         float v[32];
-                        tmem_ld32(tmem + lane_base + (side == 0 ? TM_DEI : TM_DEJ) + half * 32, v);
+                        tmem_ld32(tmem + lane_base + buf * 256 + a * 64 + half * 32, v);
                         const int col0 = dc * BK + half * 32;
 #pragma unroll
                         for (int h16 = 0; h16 < 2; ++h16) {
@@ -440,10 +533,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                             for (int m = 0; m < 4; ++m) {
                                 const int r = m * 8 + (lane >> 2), k = lane & 3;
                                 const int kk = k ^ ((r >> 1) & 3);
-                                const float4 x = *reinterpret_cast<const float4 *>(&sm.stage_t[quad][r * 16 + kk * 4]);
+                                const float4 xv = *reinterpret_cast<const float4 *>(&sm.stage_t[ew][r * 16 + kk * 4]);
                                 const int grow = row0 + r, gcol = col0 + h16 * 16 + k * 4;
                                 if (grow < P.n && gcol < P.width)
-                                    red_add_v4(P.d_e + static_cast<long long>(grow) * P.ld_de + gcol, x.x, x.y, x.z, x.w);
+                                    red_add_v4(P.d_e + static_cast<long long>(grow) * P.ld_de + gcol, xv.x, xv.y, xv.z, xv.w);
                             }
                             __syncwarp();
                         }
@@ -451,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.de_free);
+                if (lane == 0) mbar_arrive(&sm.de_free[buf]);
             }
             if (!ok) break;
         }
@@ -466,15 +559,18 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // ----------------------------------------------------------------------------
-// final scalar reduction: fixed order, float64
+// final scalar reduction: fixed order, float64, two levels
 // ----------------------------------------------------------------------------
 
-__global__ void finish_kernel(const float *partials, long long slots, int n, float *loss, float *dt, float *db,
-                              int32_t *status) {
+// Block g sums the slots of its contiguous range (thread k adds k, k + 256, ...
+// of the range, then a fixed-shape tree).
+__global__ void finish_partial_kernel(const float *partials, long long slots, double *sums, const int32_t *status) {
     if (read_status(status) != 0) return;
     __shared__ double red[3][256];
+    const long long per = (slots + gridDim.x - 1) / gridDim.x;
+    const long long lo = blockIdx.x * per, hi = min(slots, lo + per);
     double l = 0, gs = 0, g = 0;
-    for (long long s = threadIdx.x; s < slots; s += blockDim.x) {
+    for (long long s = lo + threadIdx.x; s < hi; s += blockDim.x) {
         l += partials[s * 4 + 0];
         gs += partials[s * 4 + 1];
         g += partials[s * 4 + 2];
@@ -482,6 +578,20 @@ __global__ void finish_kernel(const float *partials, long long slots, int n, flo
     red[0][threadIdx.x] = l;
     red[1][threadIdx.x] = gs;
     red[2][threadIdx.x] = g;
+    __syncthreads();
+    for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w)
+            for (int c = 0; c < 3; ++c) red[c][threadIdx.x] += red[c][threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0)
+        for (int c = 0; c < 3; ++c) sums[blockIdx.x * 3 + c] = red[c][0];
+}
+
+__global__ void finish_kernel(const double *sums, int n, float *loss, float *dt, float *db, const int32_t *status) {
+    if (read_status(status) != 0) return;
+    __shared__ double red[3][kFinishBlocks];
+    for (int c = 0; c < 3; ++c) red[c][threadIdx.x] = sums[threadIdx.x * 3 + c];
     __syncthreads();
     for (int w = blockDim.x / 2; w > 0; w >>= 1) {
         if (threadIdx.x < w)
@@ -496,15 +606,23 @@ __global__ void finish_kernel(const float *partials, long long slots, int n, flo
     }
 }
 
+long long block_count(int n) {
+    const long long nb = (n + BM - 1) / BM, nbb = (nb + 1) / 2;
+    return nbb * (nbb + 1) / 2;
+}
+
 }  // namespace pooled
 
 size_t pooled_fused_smem_bytes() { return pooled::kSmemBytes; }
+
+long long pooled_partial_slots(int n) { return pooled::block_count(n) * pooled::kPartialsPerBlock; }
+int pooled_finish_blocks() { return pooled::kFinishBlocks; }
 
 cudaError_t launch_pooled_fused(const CUtensorMap &tmap_e, const PooledLaunch &L, cudaStream_t stream) {
     using namespace pooled;
     static bool configured = false;
     if (!configured) {
-        cudaError_t err = cudaFuncSetAttribute(fused_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t err = cudaFuncSetAttribute(fused_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(kSmemBytes));
         if (err != cudaSuccess) return err;
         configured = true;
@@ -514,7 +632,8 @@ cudaError_t launch_pooled_fused(const CUtensorMap &tmap_e, const PooledLaunch &L
     P.width = L.width;
     P.nk = (L.width + BK - 1) / BK;
     P.nb = (L.n + BM - 1) / BM;
-    P.tile_pairs = static_cast<long long>(P.nb) * (P.nb + 1) / 2;
+    P.nbb = (P.nb + 1) / 2;
+    P.blocks = block_count(L.n);
     P.t_ptr = L.t_ptr;
     P.b_ptr = L.b_ptr;
     P.ambient = L.ambient;
@@ -525,18 +644,15 @@ cudaError_t launch_pooled_fused(const CUtensorMap &tmap_e, const PooledLaunch &L
     P.ld_de = L.ld_de;
     P.partials = L.partials;
     P.status = L.status;
-    long long grid = static_cast<long long>(L.sm_count) * 2;
-    if (grid > P.tile_pairs) grid = P.tile_pairs;
-    fused_tiles_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tmap_e, P);
+    long long grid = static_cast<long long>(L.sm_count);
+    if (grid > P.blocks) grid = P.blocks;
+    fused_blocks_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tmap_e, P);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    finish_kernel<<<1, 256, 0, stream>>>(L.partials, P.tile_pairs * 4, L.n, L.loss, L.dt, L.db, L.status);
+    finish_partial_kernel<<<kFinishBlocks, 256, 0, stream>>>(L.partials, P.blocks * kPartialsPerBlock, L.sums, L.status);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    finish_kernel<<<1, kFinishBlocks, 0, stream>>>(L.sums, L.n, L.loss, L.dt, L.db, L.status);
     return cudaGetLastError();
-}
-
-long long pooled_tile_pairs(int n) {
-    long long nb = (n + pooled::BM - 1) / pooled::BM;
-    return nb * (nb + 1) / 2;
 }
 
 }  // namespace cli

@@ -273,8 +273,9 @@ PooledWorkspace carve_pooled_workspace(void *base, size_t n, size_t width, size_
     w.rel_cnt = reinterpret_cast<uint32_t *>(take(n * sizeof(uint32_t)));
     w.rel_off = reinterpret_cast<uint32_t *>(take((n + 1) * sizeof(uint32_t)));
     w.rel = reinterpret_cast<RelEntry *>(take((2 * edges_total + n) * sizeof(RelEntry)));
-    w.partials = reinterpret_cast<float *>(take(static_cast<size_t>(pooled_tile_pairs(static_cast<int>(n))) * 16 *
-                                                sizeof(float)));
+    w.partials = reinterpret_cast<float *>(
+        take(static_cast<size_t>(pooled_partial_slots(static_cast<int>(n))) * 4 * sizeof(float)));
+    w.sums = reinterpret_cast<double *>(take(static_cast<size_t>(pooled_finish_blocks()) * 3 * sizeof(double)));
     w.bytes = off;
     return w;
 }
