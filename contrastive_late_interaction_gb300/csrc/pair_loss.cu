@@ -13,8 +13,9 @@
 // J0 + 1 (on a diagonal block the columns are the rows, and the mirrored tile
 // (I1, I0) is skipped).  One persistent CTA per SM; for each block:
 //   1. S pass.  tcgen05 computes the four tiles S_xy = E_Ix E_Jy^T into the
-//      512 TMEM columns (bf16 operands staged by TMA in 128-byte-swizzled
-//      128 x 64 boxes, fp32 accumulation).  The four boxes of one K step fill
+//      512 TMEM columns, as one M = 128, N = 256 product per tile row (bf16
+//      operands staged by TMA in 128-byte-swizzled 128 x 64 boxes, fp32
+//      accumulation).  The four boxes of one K step fill
 //      a stage; the shared memory that holds H later is lent to the pass as
 //      two more stages.
 //   2. Epilogue.  Eight warps read S from TMEM, one row per thread (two warps
@@ -30,7 +31,9 @@
 //      in four TMEM accumulators (two on a diagonal block, where the rows and
 //      columns coincide), reading H and the E boxes in both K-major and
 //      MN-major form from the same bytes; the epilogue warps add each chunk
-//      into dE (fp32) with vector reductions while the next chunk's MMAs run.
+//      into dE (fp32) while the next chunk's MMAs run, each vector reduction
+//      covering 128 contiguous bytes of four rows after a transpose through
+//      shared memory (the L2 reductions cost per request, not per byte).
 // Each accumulator sums the contributions of two tiles before it leaves the
 // SM, so per FLOP half as many fp32 partials reach L2 as with single tile
 // pairs: L2 reductions of dE are what bound this kernel.  Neither S nor H ever
@@ -54,15 +57,16 @@ constexpr uint32_t BOX_BYTES = BM * BK * 2;   // 16 KB
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2..9 epilogue
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int kStages = 3;              // stage 0: the box ring; stages 1, 2: the H region, lent to the S pass
+constexpr int kStages = 3;              // stage 0: the box ring (two halves); stages 1, 2: the H region, lent to the S pass
 constexpr int kPartialsPerBlock = kEpiWarps;
 constexpr int kFinishBlocks = 256;
 
 struct SharedStorage {
     alignas(1024) uint8_t ring[4][BOX_BYTES];   // stage 0: boxes of I0, I1, J0, J1
     alignas(1024) uint8_t hreg[8][BOX_BYTES];   // H tiles 0..3 (two boxes each); stages 1 and 2 of the S pass
-    alignas(16) float stage_t[kEpiWarps][32 * 16];   // per epilogue warp: 32 rows x 16 fp32, transposed drain
-    uint64_t full[kStages], empty[kStages];
+    alignas(16) float stage_t[kEpiWarps][32 * 32];   // per epilogue warp: 32 rows x 32 fp32, transposed drain
+    uint64_t full[kStages], empty[kStages];   // H-region stages 1 and 2 (index 0 unused)
+    uint64_t ring_full[2], ring_empty[2];     // ring halves: 0 = boxes of I0, I1; 1 = of J0, J1
     uint64_t s_full, h_ready, h_free, de_full[2], de_free[2], mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -227,7 +231,8 @@ __device__ __forceinline__ void red_add_v4(float *gptr, float a, float b, float 
 }
 
 // Default cells of one 32-column chunk: accumulate the sums and write H.
-template <bool kFar>
+// kFull: every row and column of the warp's chunk lies inside the batch.
+template <bool kFar, bool kFull>
 __device__ __forceinline__ void default_cells(const float (&v)[32], float t, float b, bool row_ok, int valid,
                                               float hscale, float &acc_sp, float &acc_p, float &acc_ps,
                                               float (&hv)[32]) {
@@ -236,12 +241,40 @@ __device__ __forceinline__ void default_cells(const float (&v)[32], float t, flo
         const float s = v[r];
         const float z = fmaf(t, s, b);
         const CellFn f = kFar ? cell_fn_far(z) : cell_fn(z);
-        const bool ok_col = row_ok && r < valid;
-        acc_sp += ok_col ? f.sp : 0.f;
-        acc_p += ok_col ? f.p : 0.f;
-        acc_ps += ok_col ? f.p * s : 0.f;
-        hv[r] = ok_col ? hscale * f.p : 0.f;
+        if (kFull) {
+            acc_sp += f.sp;
+            acc_p += f.p;
+            acc_ps = fmaf(f.p, s, acc_ps);
+            hv[r] = hscale * f.p;
+        } else {
+            const bool ok_col = row_ok && r < valid;
+            acc_sp += ok_col ? f.sp : 0.f;
+            acc_p += ok_col ? f.p : 0.f;
+            acc_ps += ok_col ? f.p * s : 0.f;
+            hv[r] = ok_col ? hscale * f.p : 0.f;
+        }
     }
+}
+
+// Default cells of a full chunk where every z <= -kFarZ (the common repel
+// cell): e = exp(z) < 2^-7, sigma(z) = e - e^2 and softplus(z) = e - e^2/2,
+// each to relative error below e^2 < 2^-14.  The chunk's sums of e and e^2
+// give those of sigma and softplus; one MUFU op per cell.
+__device__ __forceinline__ void default_cells_negfar(const float (&v)[32], float t2, float b2, float hscale,
+                                                     float &acc_sp, float &acc_p, float &acc_ps, float (&hv)[32]) {
+    float se = 0.f, se2 = 0.f;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+        const float s = v[r];
+        const float e = fast_ex2(fmaf(t2, s, b2));   // exp(z) with t2 = t log2(e), b2 = b log2(e)
+        const float p = fmaf(-e, e, e);
+        se += e;
+        se2 = fmaf(e, e, se2);
+        acc_ps = fmaf(p, s, acc_ps);
+        hv[r] = hscale * p;
+    }
+    acc_sp += fmaf(-0.5f, se2, se);
+    acc_p += se - se2;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -257,6 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1);
+        }
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&sm.ring_full[h], 1);
+            mbar_init(&sm.ring_empty[h], 1);
         }
         mbar_init(&sm.s_full, 1);
         mbar_init(&sm.h_ready, kEpiWarps);
@@ -282,43 +319,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            uint32_t ph = 0;   // bit s: parity of stage s's next use
+            uint32_t ph = 0;   // bit s (1, 2): parity of H-region stage s's next use; bit 3 + h: of ring half h
             uint32_t kblk = 0;
             bool ok = true;
+            // Ring half h holds the boxes of positions 2h and 2h + 1 (h = 0: I0, I1; h = 1: J0, J1).
+            auto load_half = [&](const Block &bk, int h, int k0) -> bool {
+                const int bit = 3 + h;
+                if (!mbar_wait(&sm.ring_empty[h], ((ph >> bit) & 1) ^ 1, abort_flag, P.status, kSleepProducer)) return false;
+                const int nbox = (box_on(bk, 2 * h) ? 1 : 0) + (box_on(bk, 2 * h + 1) ? 1 : 0);
+                mbar_arrive_expect_tx(&sm.ring_full[h], nbox * BOX_BYTES);   // none on a diagonal block's J half
+                for (int pos = 2 * h; pos < 2 * h + 2; ++pos)
+                    if (box_on(bk, pos)) tma_load_2d(sm.ring[pos], &tmap_e, &sm.ring_full[h], k0, box_tile(bk, pos) * BM);
+                ph ^= 1u << bit;
+                return true;
+            };
             for (long long p = blockIdx.x; p < P.blocks && ok; p += gridDim.x, ++kblk) {
                 const Block bk = decode_block(p, P);
                 int nbox = 0;
                 for (int pos = 0; pos < 4; ++pos) nbox += box_on(bk, pos) ? 1 : 0;
                 bool h_owned = false;
-                for (int pass = 0; pass < 2 && ok; ++pass) {   // S pass, then the gradient pass
-                    for (int kc = 0; kc < P.nk; ++kc) {
-                        const int s = pass == 0 ? kc % kStages : 0;
-                        if (s != 0 && !h_owned) {
-                            // The H region holds the previous block's H until its gradient MMAs are done.
-                            if (!mbar_wait(&sm.h_free, (kblk & 1) ^ 1, abort_flag, P.status, kSleepProducer)) { ok = false; break; }
-                            h_owned = true;
-                        }
-                        if (!mbar_wait(&sm.empty[s], ((ph >> s) & 1) ^ 1, abort_flag, P.status, kSleepProducer)) { ok = false; break; }
-                        mbar_arrive_expect_tx(&sm.full[s], nbox * BOX_BYTES);
-                        for (int pos = 0; pos < 4; ++pos)
-                            if (box_on(bk, pos))
-                                tma_load_2d(box_ptr(s, pos), &tmap_e, &sm.full[s], kc * BK, box_tile(bk, pos) * BM);
-                        ph ^= 1u << s;
+                // S pass: stage kc % 3, stage 0 being both ring halves.
+                for (int kc = 0; kc < P.nk && ok; ++kc) {
+                    const int s = kc % kStages;
+                    if (s == 0) {
+                        ok = load_half(bk, 0, kc * BK) && load_half(bk, 1, kc * BK);
+                        continue;
                     }
+                    if (!h_owned) {
+                        // The H region holds the previous block's H until its gradient MMAs are done.
+                        if (!mbar_wait(&sm.h_free, (kblk & 1) ^ 1, abort_flag, P.status, kSleepProducer)) { ok = false; break; }
+                        h_owned = true;
+                    }
+                    if (!mbar_wait(&sm.empty[s], ((ph >> s) & 1) ^ 1, abort_flag, P.status, kSleepProducer)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&sm.full[s], nbox * BOX_BYTES);
+                    for (int pos = 0; pos < 4; ++pos)
+                        if (box_on(bk, pos))
+                            tma_load_2d(box_ptr(s, pos), &tmap_e, &sm.full[s], kc * BK, box_tile(bk, pos) * BM);
+                    ph ^= 1u << s;
                 }
+                // Gradient pass: the J half first, which the row-side products read first, so that
+                // each half loads while the other half's products run.
+                for (int dc = 0; dc < P.nk && ok; ++dc) ok = load_half(bk, 1, dc * BK) && load_half(bk, 0, dc * BK);
             }
             // Let in-flight loads land before the CTA can exit.
-            for (int s = 0; s < kStages; ++s) mbar_wait(&sm.empty[s], ((ph >> s) & 1) ^ 1, abort_flag, P.status);
+            for (int s = 1; s < kStages; ++s) mbar_wait(&sm.empty[s], ((ph >> s) & 1) ^ 1, abort_flag, P.status);
+            for (int h = 0; h < 2; ++h) mbar_wait(&sm.ring_empty[h], ((ph >> (3 + h)) & 1) ^ 1, abort_flag, P.status);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
+            const uint32_t idesc_s = idesc_bf16(128, 256, 0, 0);
             const uint32_t idesc_row = idesc_bf16(128, 64, 0, 1);   // A = H (K-major), B = E_J (MN-major)
             const uint32_t idesc_col = idesc_bf16(128, 64, 1, 1);   // A = H^T (MN-major), B = E_I (MN-major)
-            uint32_t ph = 0;   // bit s: parity of stage s's next use
+            uint32_t ph = 0;   // bit s (1, 2): parity of H-region stage s's next use; bit 3 + h: of ring half h
             uint32_t kblk = 0, chunk = 0;
             bool ok = true;
+            auto wait_half = [&](int h) -> bool {
+                return mbar_wait(&sm.ring_full[h], (ph >> (3 + h)) & 1, abort_flag, P.status, kSleepIssuer);
+            };
+            auto free_half = [&](int h) {
+                mma_commit(&sm.ring_empty[h]);
+                ph ^= 1u << (3 + h);
+            };
             for (long long p = blockIdx.x; p < P.blocks && ok; p += gridDim.x, ++kblk) {
                 const Block bk = decode_block(p, P);
                 // S takes every TMEM column: wait until the last gradient chunk has been drained.
@@ -328,21 +390,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 for (int kc = 0; kc < P.nk; ++kc) {
                     const int s = kc % kStages;
-                    if (!mbar_wait(&sm.full[s], (ph >> s) & 1, abort_flag, P.status, kSleepIssuer)) { ok = false; break; }
+                    if (s == 0 ? !(wait_half(0) && wait_half(1))
+                               : !mbar_wait(&sm.full[s], (ph >> s) & 1, abort_flag, P.status, kSleepIssuer)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
+                    // One N = 256 MMA per tile row: the boxes of J0 and J1 (I0 and I1 on a diagonal
+                    // block) are adjacent, so together they are one 256-row K-major operand whose
+                    // product fills the TMEM columns of slots (x, 0) and (x, 1).  A slot that is
+                    // off (an absent J1, or (1, 0) on a diagonal block) is computed from whatever
+                    // the unloaded box holds and never read.
 #pragma unroll
-                    for (int x = 0; x < 2; ++x)
+                    for (int x = 0; x < 2; ++x) {
+                        if (x == 1 && !bk.i1) continue;
+                        const uint32_t a = smem_u32(box_ptr(s, x)), b = smem_u32(box_ptr(s, col_pos(bk, 0)));
 #pragma unroll
-                        for (int y = 0; y < 2; ++y) {
-                            if (!slot_on(bk, x, y)) continue;
-                            const uint32_t a = smem_u32(box_ptr(s, x)), b = smem_u32(box_ptr(s, col_pos(bk, y)));
-#pragma unroll
-                            for (int kk = 0; kk < BK / 16; ++kk)
-                                mma_bf16(tmem + (2 * x + y) * BM, sdesc_sw128(a + kk * 32, 16, 1024),
-                                         sdesc_sw128(b + kk * 32, 16, 1024), idesc_s, (kc | kk) != 0);
-                        }
-                    mma_commit(&sm.empty[s]);
-                    ph ^= 1u << s;
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            mma_bf16(tmem + x * 2 * BM, sdesc_sw128(a + kk * 32, 16, 1024), sdesc_sw128(b + kk * 32, 16, 1024),
+                                     idesc_s, (kc | kk) != 0);
+                    }
+                    if (s == 0) {
+                        free_half(0);
+                        free_half(1);
+                    } else {
+                        mma_commit(&sm.empty[s]);
+                        ph ^= 1u << s;
+                    }
                 }
                 if (!ok) break;
                 mma_commit(&sm.s_full);
@@ -351,38 +425,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 for (int dc = 0; dc < P.nk; ++dc, ++chunk) {
                     const uint32_t buf = chunk & 1;
-                    if (!mbar_wait(&sm.full[0], ph & 1, abort_flag, P.status, kSleepIssuer)) { ok = false; break; }
                     if (!mbar_wait(&sm.de_free[buf], ((chunk >> 1) & 1) ^ 1, abort_flag, P.status, kSleepIssuer)) { ok = false; break; }
-                    tc_fence_after();
                     const uint32_t acc0 = tmem + buf * 256;
                     uint32_t started = 0;   // bit a: accumulator a holds this chunk's first product
+                    // Row side: acc[x] += H_xy E_Jy.  A: H rows i, K = j (16 per step) inside 64-wide
+                    // K blocks; B: the E_Jy box viewed as [N = 64 features] x [K = j].
+                    auto row_side = [&]() {
+#pragma unroll
+                        for (int x = 0; x < 2; ++x)
+#pragma unroll
+                            for (int y = 0; y < 2; ++y) {
+                                if (!slot_on(bk, x, y)) continue;
+                                const uint32_t h = smem_u32(sm.hreg[2 * (2 * x + y)]);
+                                const uint32_t ej = smem_u32(sm.ring[col_pos(bk, y)]);
+#pragma unroll
+                                for (int kk = 0; kk < BM / 16; ++kk)
+                                    mma_bf16(acc0 + x * 64, sdesc_sw128(h + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024),
+                                             sdesc_sw128(ej + kk * 2048, 1024, 1024), idesc_row,
+                                             ((started >> x) & 1) || kk != 0);
+                                started |= 1u << x;
+                            }
+                    };
+                    if (!wait_half(1)) { ok = false; break; }
+                    tc_fence_after();
+                    if (!bk.diag) row_side();
+                    free_half(1);
+                    if (!wait_half(0)) { ok = false; break; }
+                    tc_fence_after();
+                    if (bk.diag) row_side();   // on a diagonal block the column tiles are I0, I1
+                    // Column side: acc[col] += H_xy^T E_Ix.  A: H viewed as [M = j] x [K = i], j
+                    // contiguous within a 64-wide block (blocks BOX_BYTES apart), 8 rows of i per 1024
+                    // bytes.  A diagonal tile's H is symmetric: its row side is all of it.
 #pragma unroll
                     for (int x = 0; x < 2; ++x)
 #pragma unroll
                         for (int y = 0; y < 2; ++y) {
-                            if (!slot_on(bk, x, y)) continue;
+                            if (!slot_on(bk, x, y) || (bk.diag && x == y)) continue;
                             const uint32_t h = smem_u32(sm.hreg[2 * (2 * x + y)]);
-                            // Row side: acc[x] += H_xy E_Jy.  A: H rows i, K = j (16 per step) inside
-                            // 64-wide K blocks; B: the E_Jy box viewed as [N = 64 features] x [K = j].
-                            const uint32_t ej = smem_u32(box_ptr(0, col_pos(bk, y)));
-#pragma unroll
-                            for (int kk = 0; kk < BM / 16; ++kk)
-                                mma_bf16(acc0 + x * 64, sdesc_sw128(h + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024),
-                                         sdesc_sw128(ej + kk * 2048, 1024, 1024), idesc_row, ((started >> x) & 1) || kk != 0);
-                            started |= 1u << x;
-                            if (bk.diag && x == y) continue;   // a diagonal tile: H is symmetric, the row side is all
-                            // Column side: acc[col] += H_xy^T E_Ix.  A: H viewed as [M = j] x [K = i], j
-                            // contiguous within a 64-wide block (blocks BOX_BYTES apart), 8 rows of i per 1024 bytes.
                             const int ca = col_pos(bk, y);
-                            const uint32_t ei = smem_u32(box_ptr(0, x));
+                            const uint32_t ei = smem_u32(sm.ring[x]);
 #pragma unroll
                             for (int kk = 0; kk < BM / 16; ++kk)
                                 mma_bf16(acc0 + ca * 64, sdesc_sw128(h + kk * 2048, BOX_BYTES, 1024),
                                          sdesc_sw128(ei + kk * 2048, 1024, 1024), idesc_col, ((started >> ca) & 1) || kk != 0);
                             started |= 1u << ca;
                         }
-                    mma_commit(&sm.empty[0]);
-                    ph ^= 1u;
+                    free_half(0);
                     mma_commit(&sm.de_full[buf]);
                 }
                 if (!ok) break;
@@ -399,6 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quad * 32 + lane;        // row of the tile this thread owns
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const float t = *P.t_ptr, b = *P.b_ptr;
+        const float t2 = t * kLog2e, b2 = b * kLog2e;
         const float inv_n = 1.0f / static_cast<float>(P.n);
         const float c_h = t * inv_n;             // H = (t/N) G
         const float w_d = P.named ? 0.0f : P.ambient;
@@ -439,15 +528,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(tmem + lane_base + slot * BM + ch * 32, v);
                     const int c0 = j0 + ch * 32;
                     const int valid = min(32, P.n - c0);   // columns of this chunk inside the batch
-                    float zmin = 3.0e38f;
+                    // The chunk's range of z (t may be negative) picks the cheapest exact-enough path.
+                    float smin = v[0], smax = v[0];
 #pragma unroll
-                    for (int r = 0; r < 32; ++r) zmin = fminf(zmin, fabsf(fmaf(t, v[r], b)));
+                    for (int r = 1; r < 32; ++r) {
+                        smin = fminf(smin, v[r]);
+                        smax = fmaxf(smax, v[r]);
+                    }
+                    const float za = fmaf(t, smin, b), zb = fmaf(t, smax, b);
+                    const float zlo = fminf(za, zb), zhi = fmaxf(za, zb);
                     float hv[32];
                     const float hscale = c_h * 2.0f * w_d;
-                    if (__all_sync(0xffffffffu, zmin >= kFarZ))
-                        default_cells<true>(v, t, b, row_ok, valid, hscale, acc_sp, acc_p, acc_ps, hv);
+                    const bool full = __all_sync(0xffffffffu, row_ok && valid == 32);
+                    const bool negfar = __all_sync(0xffffffffu, zhi <= -kFarZ);
+                    const bool far = __all_sync(0xffffffffu, zhi <= -kFarZ || zlo >= kFarZ);
+                    if (negfar && full)
+                        default_cells_negfar(v, t2, b2, hscale, acc_sp, acc_p, acc_ps, hv);
+                    else if (far && full)
+                        default_cells<true, true>(v, t, b, row_ok, valid, hscale, acc_sp, acc_p, acc_ps, hv);
+                    else if (far)
+                        default_cells<true, false>(v, t, b, row_ok, valid, hscale, acc_sp, acc_p, acc_ps, hv);
+                    else if (full)
+                        default_cells<false, true>(v, t, b, row_ok, valid, hscale, acc_sp, acc_p, acc_ps, hv);
                     else
-                        default_cells<false>(v, t, b, row_ok, valid, hscale, acc_sp, acc_p, acc_ps, hv);
+                        default_cells<false, false>(v, t, b, row_ok, valid, hscale, acc_sp, acc_p, acc_ps, hv);
                     // Special cells: replace the default by the resolved pair of directions.
                     while (e < e_end) {
                         const RelEntry en = P.rel[e];
@@ -512,34 +616,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int a = x; a < 4; a += 2) {
                     if (!box_on(bk, a)) continue;   // warp-uniform: the accumulator of an absent tile row
                     const int row0 = box_tile(bk, a) * BM + quad * 32;   // first row of this warp's 32
-#pragma unroll
+#pragma unroll 1
                     for (int half = 0; half < 2; ++half) {
                         float v[32];
                         tmem_ld32(tmem + lane_base + buf * 256 + a * 64 + half * 32, v);
-                        const int col0 = dc * BK + half * 32;
+                        // lane = row: its 32 values as 8 x 16 B, chunk index swizzled by row
 #pragma unroll
-                        for (int h16 = 0; h16 < 2; ++h16) {
-                            // lane = row: write 16 values (4 x 16 B, chunk index swizzled by row)
+                        for (int k = 0; k < 8; ++k)
+                            st_shared_v4(stage_s + (lane * 32 + ((k ^ (lane & 7)) * 4)) * 4, __float_as_uint(v[k * 4]),
+                                         __float_as_uint(v[k * 4 + 1]), __float_as_uint(v[k * 4 + 2]),
+                                         __float_as_uint(v[k * 4 + 3]));
+                        __syncwarp();
+                        // read back: instruction m covers rows 4m .. 4m+3, 8 lanes x 16 B = 128 B per row
+                        const int col = dc * BK + half * 32 + (lane & 7) * 4;
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const int kk = k ^ ((lane >> 1) & 3);
-                                st_shared_v4(stage_s + (lane * 16 + kk * 4) * 4, __float_as_uint(v[h16 * 16 + k * 4]),
-                                             __float_as_uint(v[h16 * 16 + k * 4 + 1]), __float_as_uint(v[h16 * 16 + k * 4 + 2]),
-                                             __float_as_uint(v[h16 * 16 + k * 4 + 3]));
-                            }
-                            __syncwarp();
-                            // read back: instruction m covers rows 8m .. 8m+7, 4 lanes x 16 B per row
-#pragma unroll
-                            for (int m = 0; m < 4; ++m) {
-                                const int r = m * 8 + (lane >> 2), k = lane & 3;
-                                const int kk = k ^ ((r >> 1) & 3);
-                                const float4 xv = *reinterpret_cast<const float4 *>(&sm.stage_t[ew][r * 16 + kk * 4]);
-                                const int grow = row0 + r, gcol = col0 + h16 * 16 + k * 4;
-                                if (grow < P.n && gcol < P.width)
-                                    red_add_v4(P.d_e + static_cast<long long>(grow) * P.ld_de + gcol, xv.x, xv.y, xv.z, xv.w);
-                            }
-                            __syncwarp();
+                        for (int m = 0; m < 8; ++m) {
+                            const int r = m * 4 + (lane >> 3);
+                            const float4 xv = *reinterpret_cast<const float4 *>(&sm.stage_t[ew][r * 32 + (((lane & 7) ^ (r & 7)) * 4)]);
+                            const int grow = row0 + r;
+                            if (grow < P.n && col < P.width)
+                                red_add_v4(P.d_e + static_cast<long long>(grow) * P.ld_de + col, xv.x, xv.y, xv.z, xv.w);
                         }
+                        __syncwarp();
                     }
                 }
                 tc_fence_before();

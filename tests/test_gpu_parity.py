@@ -70,6 +70,17 @@ def test_pooled_ragged_weighted(n, width, named):
     assert torch.all(pad == 7.0), "columns past the width were written"
 
 
+@pytest.mark.parametrize("t,b", [(10.0, 10.0), (-10.0, -10.0), (1.0, 0.0), (-4.0, 6.0)])
+def test_pooled_score_regimes(t, b):
+    """Every regime of z = t s + b the epilogue distinguishes: all cells far positive, far negative with a
+    negative temperature, near zero, and a mix."""
+    p = synth.pooled_bags(5, 300, 64, ignore_p=0.01)
+    p.t, p.b = t, b
+    g = run_pooled(p)
+    ref = oracle.pair_loss_sigmoid(p.e_rounded, t, b, p.attract, None, p.ignore, p.negatives_named, p.ambient_weight)
+    compare_pooled(p, g, ref)
+
+
 def test_pooled_config4_sampled_rows_and_invariance():
     """N=32768, D=768, bags of four: sampled dE rows against the oracle's per-anchor gradient; L, dt and
     db against a second run with the items permuted (the loss is invariant, dE permutes)."""
