@@ -366,20 +366,24 @@ __global__ void qmap_kernel(const uint64_t *q_off, int nq, int32_t *qmap, const 
     for (uint64_t t = q_off[q]; t < q_off[q + 1]; ++t) qmap[t] = q;
 }
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&x)[8]) {
+// acc[i] += c * (the 8 bf16 of u), as four packed fp32 pair FMAs; u holds
+// features 2i (low half of word i) and 2i + 1 (high half).
+__device__ __forceinline__ void fma_bf16x8(float2 (&acc)[4], const uint4 u, float c) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    const float2 c2 = make_float2(c, c);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        x[2 * i] = __uint_as_float(w[i] << 16);
-        x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
+    for (int i = 0; i < 4; ++i)
+        acc[i] = __ffma2_rn(make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u)), c2, acc[i]);
 }
 
 // dQ[t] = sum_d c(q(t), d) * D[d_off[d] + argmax[d][t]]: 8 threads per query
 // row, each owning 8 features of every 64-feature block.  Documents go in
-// groups of 8 whose argmax entries, upstream gradients and offsets are loaded
-// before any of the 8 row gathers is used, so every thread keeps 8 x 16-byte
-// gathers (per feature block) in flight.
+// steps of 8: thread `sub` of the row's group resolves document d0 + sub (its
+// argmax entry, range check, row address and c) and the group shares the eight
+// results by shuffles, so each thread then spends its instructions on the
+// 16-byte gathers and packed FMAs.  The loads that resolve the next step are
+// issued before this step's gathers, so a step waits on one round trip to L2,
+// not two.
 constexpr int kDqRows = 32;
 constexpr int kDqUnroll = 8;
 template <int NBLK>   // 64-feature blocks of the width (1..4)
@@ -387,66 +391,82 @@ __global__ void __launch_bounds__(256) dq_kernel(MaxSimBwdLaunch L) {
     if (read_status(L.status) != 0) return;
     const int t = blockIdx.x * kDqRows + (threadIdx.x >> 3);
     const int sub = threadIdx.x & 7;
-    if (t >= L.rows_q) return;
-    const int q = L.qmap[t];
+    const bool row_ok = t < L.rows_q;      // rows past the tape still shuffle with their group
+    const int tc = row_ok ? t : L.rows_q - 1;
+    const int q = L.qmap[tc];
     const float scale = L.mean ? 1.0f / static_cast<float>(L.q_off[q + 1] - L.q_off[q]) : 1.0f;
-    constexpr int nblk = NBLK;
-    float acc[NBLK][8];
+    float2 acc[NBLK][4];
 #pragma unroll
     for (int k = 0; k < NBLK; ++k)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[k][i] = 0.f;
+        for (int i = 0; i < 4; ++i) acc[k][i] = make_float2(0.f, 0.f);
     const float *dsrow = L.d_scores + static_cast<long long>(q) * L.ld_ds;
-    const int32_t *amcol = L.argmax + t;
+    const int32_t *amcol = L.argmax + tc;
+    // The raw loads that resolve document d ...
+    int a_n = 0;
+    uint64_t o_n = 0, e_n = 0;
+    float c_n = 0.f;
+    auto fetch = [&](int d) {
+        if (d < L.nd) {
+            a_n = __ldg(amcol + static_cast<long long>(d) * L.ld_argmax);
+            o_n = __ldg(L.d_off + d);
+            e_n = __ldg(L.d_off + d + 1);
+            c_n = __ldg(dsrow + d);
+        }
+    };
+    // ... and their use: the gathered row (0 past the last document or for a rejected entry) and c.
+    auto finish = [&](int d, unsigned long long &src, float &c) {
+        src = 0;
+        c = 0.f;
+        if (d < L.nd) {
+            if (a_n < 0 || static_cast<uint64_t>(a_n) >= e_n - o_n) {
+                if (row_ok) report(L.status, CLI_MALFORMED);
+            } else {
+                src = reinterpret_cast<unsigned long long>(L.d + (o_n + static_cast<uint64_t>(a_n)) * L.width);
+                c = c_n * scale;
+            }
+        }
+    };
+    unsigned long long src;
+    float c;
+    fetch(sub);
+    finish(sub, src, c);
     for (int d0 = 0; d0 < L.nd; d0 += kDqUnroll) {
-        int a[kDqUnroll];
-        float c[kDqUnroll];
-        uint64_t o[kDqUnroll + 1];
+        fetch(d0 + kDqUnroll + sub);   // the next step's resolution, in flight during this step
+        unsigned long long su[kDqUnroll];
+        float cu[kDqUnroll];
 #pragma unroll
         for (int u = 0; u < kDqUnroll; ++u) {
-            const int d = d0 + u;
-            a[u] = d < L.nd ? __ldg(amcol + static_cast<long long>(d) * L.ld_argmax) : 0;
-            c[u] = d < L.nd ? __ldg(dsrow + d) * scale : 0.f;
+            su[u] = __shfl_sync(0xffffffffu, src, u, 8);
+            cu[u] = __shfl_sync(0xffffffffu, c, u, 8);
         }
-#pragma unroll
-        for (int u = 0; u <= kDqUnroll; ++u) o[u] = __ldg(L.d_off + min(d0 + u, L.nd));
+        // Unconditional loads (a missing row reads row 0 of the tape, a feature block past the
+        // width its last 8 features), masked afterwards: nothing branches between the gathers.
         uint4 x[kDqUnroll][NBLK];
 #pragma unroll
         for (int u = 0; u < kDqUnroll; ++u) {
-            const uint64_t len = o[u + 1] - o[u];
-            const bool valid = d0 + u < L.nd;
-            if (valid && (a[u] < 0 || static_cast<uint64_t>(a[u]) >= len)) {
-                report(L.status, CLI_MALFORMED);
-                c[u] = 0.f;
-                a[u] = 0;
-            }
-            const uint16_t *src = L.d + (o[u] + static_cast<uint64_t>(valid ? a[u] : 0)) * L.width;
+            const uint16_t *row = su[u] != 0 ? reinterpret_cast<const uint16_t *>(su[u]) : L.d;
 #pragma unroll
-            for (int k = 0; k < NBLK; ++k) {
-                const int f = k * 64 + sub * 8;
-                x[u][k] = (valid && f < L.width) ? __ldg(reinterpret_cast<const uint4 *>(src + f))
-                                                 : make_uint4(0, 0, 0, 0);
-            }
+            for (int k = 0; k < NBLK; ++k)
+                x[u][k] = __ldg(reinterpret_cast<const uint4 *>(row + min(k * 64 + sub * 8, L.width - 8)));
         }
 #pragma unroll
-        for (int u = 0; u < kDqUnroll; ++u) {
+        for (int u = 0; u < kDqUnroll; ++u)
 #pragma unroll
             for (int k = 0; k < NBLK; ++k) {
-                float v[8];
-                bf16x8_to_f32(x[u][k], v);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[k][i] = fmaf(c[u], v[i], acc[k][i]);
+                if (su[u] == 0 || k * 64 + sub * 8 >= L.width) x[u][k] = make_uint4(0, 0, 0, 0);
+                fma_bf16x8(acc[k], x[u][k], cu[u]);
             }
-        }
+        finish(d0 + kDqUnroll + sub, src, c);
     }
-    (void)nblk;
+    if (!row_ok) return;
     float *dst = L.dq + static_cast<long long>(t) * L.width;
 #pragma unroll
     for (int k = 0; k < NBLK; ++k) {
         const int f = k * 64 + sub * 8;
         if (f < L.width) {
-            reinterpret_cast<float4 *>(dst + f)[0] = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
-            reinterpret_cast<float4 *>(dst + f)[1] = make_float4(acc[k][4], acc[k][5], acc[k][6], acc[k][7]);
+            reinterpret_cast<float4 *>(dst + f)[0] = make_float4(acc[k][0].x, acc[k][0].y, acc[k][1].x, acc[k][1].y);
+            reinterpret_cast<float4 *>(dst + f)[1] = make_float4(acc[k][2].x, acc[k][2].y, acc[k][3].x, acc[k][3].y);
         }
     }
 }
@@ -455,8 +475,9 @@ __global__ void __launch_bounds__(256) dq_kernel(MaxSimBwdLaunch L) {
 // kDsMaxRows document rows and a chunk of up to kDsChunk query rows:
 //   1. count, per document row s, the query rows whose argmax names it
 //      (shared-memory histogram), and scan the counts into bucket offsets;
-//   2. scatter the query rows into their buckets (a shared list of 16-bit
-//      row offsets);
+//   2. scatter the query rows into their buckets (a shared list of the row's
+//      offset in the chunk and, in the high half, its query, so that step 3
+//      reads c(q, d) from the shared table without a global lookup);
 //   3. warps take document rows dynamically and sum c(q(t), d) * Q[t] over the
 //      row's bucket in registers, lanes as features (coalesced row gathers
 //      from the L2-resident query tape), then write the row once (the first
@@ -468,11 +489,51 @@ __global__ void __launch_bounds__(256) dq_kernel(MaxSimBwdLaunch L) {
 // runs: dD is reproducible to rounding, not bit for bit.
 constexpr int kDsThreads = 512;
 constexpr int kDsMaxRows = 4096;
-constexpr int kDsChunk = 32768;
+constexpr int kDsChunk = 16384;
 constexpr int kDsMaxTable = 4096;
 
 __host__ __device__ inline size_t ds_smem_bytes() {
-    return static_cast<size_t>(kDsMaxRows) * 4 + (kDsMaxRows + 1) * 4 + kDsChunk * 2 + kDsMaxTable * 4 + 64;
+    return static_cast<size_t>(kDsMaxRows) * 4 + (kDsMaxRows + 1) * 4 + kDsChunk * 4 + kDsMaxTable * 4 + 64;
+}
+
+// Adds c(q(t), d) * Q[t] over the bucket entries [b0, b1) into this lane's
+// accumulators: each half-warp takes every other entry, 16 lanes x 8 features
+// per 128-feature block.  kFast: the list entries name the query and c comes
+// from the shared table; otherwise the query and c come from device memory.
+template <int NB, int kUnroll, bool kFast>
+__device__ __forceinline__ void dd_bucket_sum(const MaxSimBwdLaunch &L, const uint32_t *list, const float *ctab, int d,
+                                              int c0, uint32_t b0, uint32_t b1, int half, int part,
+                                              float2 (&acc)[NB][4]) {
+    for (uint32_t e = b0; e < b1; e += 2 * kUnroll) {
+        uint4 x[kUnroll][NB];
+        float c[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint32_t ee = e + 2 * u + half;
+            const bool v = ee < b1;
+            const uint32_t ent = list[v ? ee : b0];
+            const int t = c0 + static_cast<int>(ent & 0xFFFFu);
+            float cc;
+            if (kFast) {
+                cc = ctab[ent >> 16];
+            } else {
+                const int q = __ldg(L.qmap + t);
+                cc = __ldg(L.d_scores + static_cast<long long>(q) * L.ld_ds + d);
+                if (L.mean) cc /= static_cast<float>(L.q_off[q + 1] - L.q_off[q]);
+            }
+            c[u] = v ? cc : 0.f;
+            const uint16_t *src = L.q + static_cast<long long>(t) * L.width;
+#pragma unroll
+            for (int k = 0; k < NB; ++k) {
+                const int f = k * 128 + part * 8;
+                x[u][k] = (v && f < L.width) ? __ldg(reinterpret_cast<const uint4 *>(src + f)) : make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+            for (int k = 0; k < NB; ++k) fma_bf16x8(acc[k], x[u][k], c[u]);
+    }
 }
 
 // NB: 128-feature blocks of the width (ceil(width / 128)); kDsUnroll: entry
@@ -482,7 +543,7 @@ __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch 
     extern __shared__ uint8_t ds_raw[];
     uint32_t *cnt = reinterpret_cast<uint32_t *>(ds_raw);            // [kDsMaxRows] counts, then cursors
     uint32_t *off = cnt + kDsMaxRows;                                  // [kDsMaxRows + 1] bucket starts
-    uint16_t *list = reinterpret_cast<uint16_t *>(off + kDsMaxRows + 1);  // [kDsChunk]
+    uint32_t *list = off + kDsMaxRows + 1;                             // [kDsChunk] (q << 16) | row offset
     float *ctab = reinterpret_cast<float *>(list + kDsChunk);          // [kDsMaxTable]
     uint32_t *next_row = reinterpret_cast<uint32_t *>(ctab + kDsMaxTable);
     __shared__ uint32_t warp_sums[kDsThreads / 32];
@@ -493,6 +554,7 @@ __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch 
     const int dl = static_cast<int>(L.d_off[d + 1] - o0);
     const int32_t *am = L.argmax + static_cast<long long>(d) * L.ld_argmax;
     const bool use_table = L.nq <= kDsMaxTable;
+    const bool packed = L.nq <= 65536;   // list entries carry the query as well as the row
     if (use_table)
         for (int q = threadIdx.x; q < L.nq; q += kDsThreads) {
             float c = L.d_scores[static_cast<long long>(q) * L.ld_ds + d];
@@ -501,8 +563,11 @@ __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch 
         }
     for (int w0 = 0; w0 < dl; w0 += kDsMaxRows) {
         const int wrows = min(kDsMaxRows, dl - w0);
-        for (int c0 = 0; c0 < L.rows_q; c0 += kDsChunk) {
-            const int crows = min(kDsChunk, L.rows_q - c0);
+        // Chunks of equal size (none a small remainder: every chunk pays a pass over the buckets).
+        const int n_chunks = (L.rows_q + kDsChunk - 1) / kDsChunk;
+        const int chunk_rows = (L.rows_q + n_chunks - 1) / n_chunks;
+        for (int c0 = 0; c0 < L.rows_q; c0 += chunk_rows) {
+            const int crows = min(chunk_rows, L.rows_q - c0);
             for (int r = threadIdx.x; r < wrows; r += kDsThreads) cnt[r] = 0;
             if (threadIdx.x == 0) *next_row = 0;
             __syncthreads();
@@ -554,7 +619,10 @@ __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch 
             for (int k = threadIdx.x; k < crows; k += kDsThreads) {
                 const int a = __ldg(am + c0 + k);
                 const int r = a - w0;
-                if (a >= 0 && a < dl && r >= 0 && r < wrows) list[atomicAdd(&cnt[r], 1u)] = static_cast<uint16_t>(k);
+                if (a >= 0 && a < dl && r >= 0 && r < wrows) {
+                    const uint32_t qk = packed ? (static_cast<uint32_t>(__ldg(L.qmap + c0 + k)) << 16) : 0u;
+                    list[atomicAdd(&cnt[r], 1u)] = qk | static_cast<uint32_t>(k);
+                }
             }
             __syncthreads();
             // 3. one warp per document row at a time: sum c * Q[t] over the bucket.
@@ -566,60 +634,32 @@ __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch 
                 if (lane == 0) r = atomicAdd(next_row, 1u);
                 r = __shfl_sync(0xffffffffu, r, 0);
                 if (r >= static_cast<uint32_t>(wrows)) break;
-                float acc[NB][8];
+                float2 acc[NB][4];
 #pragma unroll
                 for (int k = 0; k < NB; ++k)
 #pragma unroll
-                    for (int i2 = 0; i2 < 8; ++i2) acc[k][i2] = 0.f;
+                    for (int i2 = 0; i2 < 4; ++i2) acc[k][i2] = make_float2(0.f, 0.f);
                 const uint32_t b0 = off[r], b1 = off[r + 1];
-                for (uint32_t e = b0; e < b1; e += 2 * kDsUnroll) {
-                    uint4 x[kDsUnroll][NB];
-                    float c[kDsUnroll];
-#pragma unroll
-                    for (int u = 0; u < kDsUnroll; ++u) {
-                        const uint32_t ee = e + 2 * u + half;
-                        const bool v = ee < b1;
-                        const int t = c0 + (v ? list[ee] : 0);
-                        const int q = __ldg(L.qmap + t);
-                        float cc;
-                        if (use_table) {
-                            cc = ctab[q];
-                        } else {
-                            cc = __ldg(L.d_scores + static_cast<long long>(q) * L.ld_ds + d);
-                            if (L.mean) cc /= static_cast<float>(L.q_off[q + 1] - L.q_off[q]);
-                        }
-                        c[u] = v ? cc : 0.f;
-                        const uint16_t *src = L.q + static_cast<long long>(t) * L.width;
-#pragma unroll
-                        for (int k = 0; k < NB; ++k) {
-                            const int f = k * 128 + part * 8;
-                            x[u][k] = (v && f < L.width) ? __ldg(reinterpret_cast<const uint4 *>(src + f))
-                                                         : make_uint4(0, 0, 0, 0);
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < kDsUnroll; ++u)
-#pragma unroll
-                        for (int k = 0; k < NB; ++k) {
-                            float xv[8];
-                            bf16x8_to_f32(x[u][k], xv);
-#pragma unroll
-                            for (int i2 = 0; i2 < 8; ++i2) acc[k][i2] = fmaf(c[u], xv[i2], acc[k][i2]);
-                        }
-                }
+                if (use_table && packed)
+                    dd_bucket_sum<NB, kDsUnroll, true>(L, list, ctab, d, c0, b0, b1, half, part, acc);
+                else
+                    dd_bucket_sum<NB, kDsUnroll, false>(L, list, ctab, d, c0, b0, b1, half, part, acc);
                 // combine the two half-warps, then half 0 writes the row
 #pragma unroll
                 for (int k = 0; k < NB; ++k)
 #pragma unroll
-                    for (int i2 = 0; i2 < 8; ++i2) acc[k][i2] += __shfl_xor_sync(0xffffffffu, acc[k][i2], 16);
+                    for (int i2 = 0; i2 < 4; ++i2) {
+                        acc[k][i2].x += __shfl_xor_sync(0xffffffffu, acc[k][i2].x, 16);
+                        acc[k][i2].y += __shfl_xor_sync(0xffffffffu, acc[k][i2].y, 16);
+                    }
                 if (half == 0) {
                     float *dst = L.dd + (static_cast<long long>(o0) + w0 + r) * L.width;
 #pragma unroll
                     for (int k = 0; k < NB; ++k) {
                         const int f = k * 128 + part * 8;
                         if (f < L.width) {
-                            float4 lo = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
-                            float4 hi = make_float4(acc[k][4], acc[k][5], acc[k][6], acc[k][7]);
+                            float4 lo = make_float4(acc[k][0].x, acc[k][0].y, acc[k][1].x, acc[k][1].y);
+                            float4 hi = make_float4(acc[k][2].x, acc[k][2].y, acc[k][3].x, acc[k][3].y);
                             if (c0 > 0) {
                                 const float4 ol = reinterpret_cast<const float4 *>(dst + f)[0];
                                 const float4 oh = reinterpret_cast<const float4 *>(dst + f)[1];

@@ -156,6 +156,8 @@ def test_maxsim_tiny(mean):
     (2, 7, 50, 72, (3, 9), (1, 5)),           # many documents per tile, width not a multiple of 64
     (3, 3, 4, 256, (100, 200), (500, 900)),   # long queries and documents, the widest width
     (4, 300, 3, 8, (1, 3), (1000, 1300)),     # width 8
+    (6, 5000, 3, 64, (1, 2), (5, 40)),        # more queries than the backward's shared table of c(q, d)
+    (7, 70000, 2, 64, (1, 1), (3, 20)),       # more queries than its list entries can name
 ])
 def test_maxsim_ragged(seed, nq, nd, width, ql, dl):
     compare_maxsim_full(synth.maxsim_random(seed, nq, nd, width, ql, dl))
