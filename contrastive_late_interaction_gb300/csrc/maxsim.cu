@@ -478,40 +478,44 @@ __global__ void __launch_bounds__(256) dq_kernel(MaxSimBwdLaunch L) {
 //   2. scatter the query rows into their buckets (a shared list of the row's
 //      offset in the chunk and, in the high half, its query, so that step 3
 //      reads c(q, d) from the shared table without a global lookup);
-//   3. warps take document rows dynamically and sum c(q(t), d) * Q[t] over the
-//      row's bucket in registers, lanes as features (coalesced row gathers
-//      from the L2-resident query tape), then write the row once (the first
-//      chunk stores, later chunks add; the CTA owns the document, so no
+//   3. 8-lane groups take document rows in turn and sum c(q(t), d) * Q[t] over
+//      the row's bucket in registers, lanes as features (whole-sector row
+//      gathers from the L2-resident query tape), then write the row once (the
+//      first chunk stores, later chunks add; the CTA owns the document, so no
 //      atomics touch dD).
 // No floating-point atomics; results do not depend on scheduling order within
-// a bucket because each bucket is summed by one warp in list order, and the
+// a bucket because each bucket is summed by one group in list order, and the
 // list order is the scatter order (atomic slot claims), which may vary between
 // runs: dD is reproducible to rounding, not bit for bit.
 constexpr int kDsThreads = 512;
 constexpr int kDsMaxRows = 4096;
 constexpr int kDsChunk = 16384;
 constexpr int kDsMaxTable = 4096;
+constexpr int kDsBatch = 8;   // argmax entries per thread in flight in the histogram and scatter passes
 
 __host__ __device__ inline size_t ds_smem_bytes() {
     return static_cast<size_t>(kDsMaxRows) * 4 + (kDsMaxRows + 1) * 4 + kDsChunk * 4 + kDsMaxTable * 4 + 64;
 }
 
+// A 16-byte block of zeros in device memory: the load address of a lane with
+// nothing to gather, so the gathers need neither branches nor masks.
+__device__ const uint4 kZero16 = {0u, 0u, 0u, 0u};
+
 // Adds c(q(t), d) * Q[t] over the bucket entries [b0, b1) into this lane's
-// accumulators: each half-warp takes every other entry, 16 lanes x 8 features
-// per 128-feature block.  kFast: the list entries name the query and c comes
-// from the shared table; otherwise the query and c come from device memory.
+// accumulators (features 16 part .. 16 part + 15 of every 128-feature block;
+// acc[k][h][i] holds features 16 part + 8h + 2i, + 1 of block k), kUnroll entries
+// in flight.  kFast: the list entries name the query and c comes from the
+// shared table; otherwise the query and c come from device memory.
 template <int NB, int kUnroll, bool kFast>
-__device__ __forceinline__ void dd_bucket_sum(const MaxSimBwdLaunch &L, const uint32_t *list, const float *ctab, int d,
-                                              int c0, uint32_t b0, uint32_t b1, int half, int part,
-                                              float2 (&acc)[NB][4]) {
-    for (uint32_t e = b0; e < b1; e += 2 * kUnroll) {
-        uint4 x[kUnroll][NB];
+__device__ __forceinline__ void dd_row_sum(const MaxSimBwdLaunch &L, const uint32_t *list, const float *ctab, int d,
+                                           int c0, uint32_t b0, uint32_t b1, int part, float2 (&acc)[NB][2][4]) {
+    for (uint32_t e = b0; e < b1; e += kUnroll) {
+        uint4 x[kUnroll][NB][2];
         float c[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const uint32_t ee = e + 2 * u + half;
-            const bool v = ee < b1;
-            const uint32_t ent = list[v ? ee : b0];
+            const bool v = e + u < b1;
+            const uint32_t ent = list[v ? e + u : b0];
             const int t = c0 + static_cast<int>(ent & 0xFFFFu);
             float cc;
             if (kFast) {
@@ -524,20 +528,25 @@ __device__ __forceinline__ void dd_bucket_sum(const MaxSimBwdLaunch &L, const ui
             c[u] = v ? cc : 0.f;
             const uint16_t *src = L.q + static_cast<long long>(t) * L.width;
 #pragma unroll
-            for (int k = 0; k < NB; ++k) {
-                const int f = k * 128 + part * 8;
-                x[u][k] = (v && f < L.width) ? __ldg(reinterpret_cast<const uint4 *>(src + f)) : make_uint4(0, 0, 0, 0);
-            }
+            for (int k = 0; k < NB; ++k)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int f = k * 128 + part * 16 + h * 8;
+                    x[u][k][h] = __ldg((v && f < L.width) ? reinterpret_cast<const uint4 *>(src + f) : &kZero16);
+                }
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
 #pragma unroll
-            for (int k = 0; k < NB; ++k) fma_bf16x8(acc[k], x[u][k], c[u]);
+            for (int k = 0; k < NB; ++k) {
+                fma_bf16x8(acc[k][0], x[u][k][0], c[u]);
+                fma_bf16x8(acc[k][1], x[u][k][1], c[u]);
+            }
     }
 }
 
-// NB: 128-feature blocks of the width (ceil(width / 128)); kDsUnroll: entry
-// pairs in flight per warp.
+// NB: 128-feature blocks of the width (ceil(width / 128)); kDsUnroll: bucket
+// entries in flight per 8-lane group.
 template <int NB, int kDsUnroll>
 __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch L) {
     extern __shared__ uint8_t ds_raw[];
@@ -545,7 +554,6 @@ __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch 
     uint32_t *off = cnt + kDsMaxRows;                                  // [kDsMaxRows + 1] bucket starts
     uint32_t *list = off + kDsMaxRows + 1;                             // [kDsChunk] (q << 16) | row offset
     float *ctab = reinterpret_cast<float *>(list + kDsChunk);          // [kDsMaxTable]
-    uint32_t *next_row = reinterpret_cast<uint32_t *>(ctab + kDsMaxTable);
     __shared__ uint32_t warp_sums[kDsThreads / 32];
     if (read_status(L.status) != 0) return;
     const int d = blockIdx.x;
@@ -569,17 +577,25 @@ __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch 
         for (int c0 = 0; c0 < L.rows_q; c0 += chunk_rows) {
             const int crows = min(chunk_rows, L.rows_q - c0);
             for (int r = threadIdx.x; r < wrows; r += kDsThreads) cnt[r] = 0;
-            if (threadIdx.x == 0) *next_row = 0;
             __syncthreads();
-            // 1. histogram of the chunk's targets inside the window
-            for (int k = threadIdx.x; k < crows; k += kDsThreads) {
-                const int a = __ldg(am + c0 + k);
-                if (a < 0 || a >= dl) {
-                    report(L.status, CLI_MALFORMED);
-                    continue;
+            // 1. histogram of the chunk's targets inside the window (eight loads in flight per thread)
+            for (int k0 = threadIdx.x; k0 < crows; k0 += kDsBatch * kDsThreads) {
+                int a[kDsBatch];
+#pragma unroll
+                for (int i = 0; i < kDsBatch; ++i) {
+                    const int k = k0 + i * kDsThreads;
+                    a[i] = k < crows ? __ldg(am + c0 + k) : 0;
                 }
-                const int r = a - w0;
-                if (r >= 0 && r < wrows) atomicAdd(&cnt[r], 1u);
+#pragma unroll
+                for (int i = 0; i < kDsBatch; ++i) {
+                    if (k0 + i * kDsThreads >= crows) break;
+                    if (a[i] < 0 || a[i] >= dl) {
+                        report(L.status, CLI_MALFORMED);
+                        continue;
+                    }
+                    const int r = a[i] - w0;
+                    if (r >= 0 && r < wrows) atomicAdd(&cnt[r], 1u);
+                }
             }
             __syncthreads();
             // exclusive scan of cnt[0..wrows) into off[], then cnt[] becomes the cursor
@@ -615,62 +631,55 @@ __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch 
                 if (threadIdx.x == kDsThreads - 1) off[wrows] = run;
             }
             __syncthreads();
-            // 2. scatter the chunk's rows into their buckets
-            for (int k = threadIdx.x; k < crows; k += kDsThreads) {
-                const int a = __ldg(am + c0 + k);
-                const int r = a - w0;
-                if (a >= 0 && a < dl && r >= 0 && r < wrows) {
-                    const uint32_t qk = packed ? (static_cast<uint32_t>(__ldg(L.qmap + c0 + k)) << 16) : 0u;
-                    list[atomicAdd(&cnt[r], 1u)] = qk | static_cast<uint32_t>(k);
+            // 2. scatter the chunk's rows into their buckets (eight rows per thread at a time)
+            for (int k0 = threadIdx.x; k0 < crows; k0 += kDsBatch * kDsThreads) {
+                int a[kDsBatch];
+                uint32_t qk[kDsBatch];
+#pragma unroll
+                for (int i = 0; i < kDsBatch; ++i) {
+                    const int k = k0 + i * kDsThreads;
+                    a[i] = k < crows ? __ldg(am + c0 + k) : -1;
+                    qk[i] = (packed && k < crows) ? static_cast<uint32_t>(__ldg(L.qmap + c0 + k)) << 16 : 0u;
+                }
+#pragma unroll
+                for (int i = 0; i < kDsBatch; ++i) {
+                    const int r = a[i] - w0;
+                    if (a[i] >= 0 && a[i] < dl && r >= 0 && r < wrows)
+                        list[atomicAdd(&cnt[r], 1u)] = qk[i] | static_cast<uint32_t>(k0 + i * kDsThreads);
                 }
             }
             __syncthreads();
-            // 3. one warp per document row at a time: sum c * Q[t] over the bucket.
-            //    Each half-warp takes one bucket entry (16 lanes x 16 bytes cover
-            //    128 features per block), kDsUnroll entry pairs per iteration.
-            const int half = lane >> 4, part = lane & 15;
-            for (;;) {
-                uint32_t r = 0;
-                if (lane == 0) r = atomicAdd(next_row, 1u);
-                r = __shfl_sync(0xffffffffu, r, 0);
-                if (r >= static_cast<uint32_t>(wrows)) break;
-                float2 acc[NB][4];
+            // 3. one 8-lane group per document row (bucket): sum c * Q[t] over its entries,
+            //    lane `part` owning features 16 part .. 16 part + 15 of every 128-feature block.
+            //    The first chunk stores the row, later chunks add to it.
+            const int part = lane & 7;
+            for (int r = warp * 4 + (lane >> 3); r < wrows; r += kDsThreads / 8) {
+                float2 acc[NB][2][4];
 #pragma unroll
                 for (int k = 0; k < NB; ++k)
 #pragma unroll
-                    for (int i2 = 0; i2 < 4; ++i2) acc[k][i2] = make_float2(0.f, 0.f);
+                    for (int i2 = 0; i2 < 8; ++i2) acc[k][i2 >> 2][i2 & 3] = make_float2(0.f, 0.f);
                 const uint32_t b0 = off[r], b1 = off[r + 1];
                 if (use_table && packed)
-                    dd_bucket_sum<NB, kDsUnroll, true>(L, list, ctab, d, c0, b0, b1, half, part, acc);
+                    dd_row_sum<NB, kDsUnroll, true>(L, list, ctab, d, c0, b0, b1, part, acc);
                 else
-                    dd_bucket_sum<NB, kDsUnroll, false>(L, list, ctab, d, c0, b0, b1, half, part, acc);
-                // combine the two half-warps, then half 0 writes the row
+                    dd_row_sum<NB, kDsUnroll, false>(L, list, ctab, d, c0, b0, b1, part, acc);
+                float *dst = L.dd + (static_cast<long long>(o0) + w0 + r) * L.width;
 #pragma unroll
                 for (int k = 0; k < NB; ++k)
 #pragma unroll
-                    for (int i2 = 0; i2 < 4; ++i2) {
-                        acc[k][i2].x += __shfl_xor_sync(0xffffffffu, acc[k][i2].x, 16);
-                        acc[k][i2].y += __shfl_xor_sync(0xffffffffu, acc[k][i2].y, 16);
-                    }
-                if (half == 0) {
-                    float *dst = L.dd + (static_cast<long long>(o0) + w0 + r) * L.width;
-#pragma unroll
-                    for (int k = 0; k < NB; ++k) {
-                        const int f = k * 128 + part * 8;
+                    for (int h = 0; h < 4; ++h) {
+                        const int f = k * 128 + part * 16 + h * 4;
                         if (f < L.width) {
-                            float4 lo = make_float4(acc[k][0].x, acc[k][0].y, acc[k][1].x, acc[k][1].y);
-                            float4 hi = make_float4(acc[k][2].x, acc[k][2].y, acc[k][3].x, acc[k][3].y);
+                            const float2 p0 = acc[k][h >> 1][2 * (h & 1)], p1 = acc[k][h >> 1][2 * (h & 1) + 1];
+                            float4 v4 = make_float4(p0.x, p0.y, p1.x, p1.y);
                             if (c0 > 0) {
-                                const float4 ol = reinterpret_cast<const float4 *>(dst + f)[0];
-                                const float4 oh = reinterpret_cast<const float4 *>(dst + f)[1];
-                                lo.x += ol.x; lo.y += ol.y; lo.z += ol.z; lo.w += ol.w;
-                                hi.x += oh.x; hi.y += oh.y; hi.z += oh.z; hi.w += oh.w;
+                                const float4 o4 = *reinterpret_cast<const float4 *>(dst + f);
+                                v4.x += o4.x; v4.y += o4.y; v4.z += o4.z; v4.w += o4.w;
                             }
-                            reinterpret_cast<float4 *>(dst + f)[0] = lo;
-                            reinterpret_cast<float4 *>(dst + f)[1] = hi;
+                            *reinterpret_cast<float4 *>(dst + f) = v4;
                         }
                     }
-                }
             }
             __syncthreads();
         }
@@ -741,15 +750,15 @@ cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     const size_t ds_smem = ds_smem_bytes();
     if ((L.width + 127) / 128 == 1) {
-        if ((err = cudaFuncSetAttribute(dd_sort_kernel<1, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if ((err = cudaFuncSetAttribute(dd_sort_kernel<1, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(ds_smem))) != cudaSuccess)
             return err;
-        dd_sort_kernel<1, 8><<<L.nd, kDsThreads, ds_smem, stream>>>(L);
+        dd_sort_kernel<1, 4><<<L.nd, kDsThreads, ds_smem, stream>>>(L);
     } else {
-        if ((err = cudaFuncSetAttribute(dd_sort_kernel<2, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if ((err = cudaFuncSetAttribute(dd_sort_kernel<2, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(ds_smem))) != cudaSuccess)
             return err;
-        dd_sort_kernel<2, 3><<<L.nd, kDsThreads, ds_smem, stream>>>(L);
+        dd_sort_kernel<2, 1><<<L.nd, kDsThreads, ds_smem, stream>>>(L);
     }
     return cudaGetLastError();
 }
