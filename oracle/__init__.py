@@ -140,6 +140,48 @@ def pair_loss_sigmoid(e, t, b, attract=None, repel=None, ignore=None, negatives_
     return dict(loss=out[0], dt=out[1], db=out[2], de=de, row_loss=row_loss)
 
 
+def round_bf16(x):
+    """Nearest-even rounding of float64 values to bfloat16 (through float32), returned as float64.
+    The device scores bf16 copies of the normalised prefixes; the oracle scores the same values."""
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def pair_loss_sigmoid_matryoshka(e, prefixes, t, b, attract=None, repel=None, ignore=None, negatives_named=False,
+                                 ambient_weight=1.0, round_prefix=True, threads=None):
+    """Matryoshka prefixes under the pooled sigmoid pair loss.  Returns dict(loss, dt, db, de, per_prefix).
+
+    "Training", `uform_contrastive_t` (`matryoshka_dimensions`: ascending prefix widths, every one
+    scored) and "UForm", section "Matryoshka-Like Multi-Scale Embedders" (each prefix trained under the
+    SigLIP loss on cosine similarities).  Reading: with u_p,i = e_i[:p] / |e_i[:p]|,
+        L = sum_p L_sigmoid(u_p),  one (t, b) for every prefix,
+    and dE_i[:p] += (g_i - (g_i . u_i) u_i) / |e_i[:p]| with g = dL_p / du_p (the gradient of the
+    normalisation).  A prefix of zero norm scores the zero vector and passes no gradient.  The device
+    scores bf16 copies of u_p, so with `round_prefix` the oracle rounds u_p the same way before scoring
+    and passes the gradient through that rounding unchanged.
+    """
+    e = _f64(e)
+    n, w = e.shape
+    de = np.zeros((n, w))
+    tot = dict(loss=0.0, dt=0.0, db=0.0)
+    per = []
+    for p in prefixes:
+        x = e[:, :p]
+        norm = np.sqrt(np.sum(x * x, axis=1))
+        inv = np.divide(1.0, norm, out=np.zeros_like(norm), where=norm > 0)
+        u = x * inv[:, None]
+        r = pair_loss_sigmoid(round_bf16(u) if round_prefix else u, t, b, attract, repel, ignore, negatives_named,
+                              ambient_weight, threads=threads)
+        g = r["de"]
+        de[:, :p] += (g - np.sum(g * u, axis=1)[:, None] * u) * inv[:, None]
+        for k in tot:
+            tot[k] += r[k]
+        per.append(dict(width=p, loss=r["loss"], dt=r["dt"], db=r["db"]))
+    return dict(loss=tot["loss"], dt=tot["dt"], db=tot["db"], de=de, per_prefix=per)
+
+
 def pair_loss_sigmoid_scores(scores, t, b, attract=None, repel=None, ignore=None, sides=None,
                              negatives_named=False, ambient_weight=1.0):
     """Sigmoid pair loss over a given score matrix [R, C].  Returns dict(loss, dt, db, dscores)."""
