@@ -85,6 +85,14 @@ class PairLossSigmoidArgs(ctypes.Structure):
                 ("workspace_bytes", c_size_t), ("device_status", c_void_p), ("stream", c_void_p)]
 
 
+class PairLossMatryoshkaArgs(ctypes.Structure):
+    _fields_ = [("base", PairLossSigmoidArgs), ("prefix_widths", c_void_p), ("prefix_count", c_size_t),
+                ("prefix_loss", c_void_p)]
+
+
+MATRYOSHKA_MAX_PREFIXES = 8   # CLI_MATRYOSHKA_MAX_PREFIXES in include/cli.h
+
+
 class PairLossSigmoidScoresArgs(ctypes.Structure):
     _fields_ = [("rows", c_size_t), ("cols", c_size_t), ("ld", c_size_t), ("scores", c_void_p),
                 ("inverse_temperature", c_void_p), ("bias", c_void_p), ("relations", Relations),
@@ -122,6 +130,8 @@ EXPORTS = {
     "cli_status_name": (ctypes.c_char_p, [c_int]),
     "pair_loss_sigmoid_fwd_bwd": (c_int, [ctypes.POINTER(PairLossSigmoidArgs)]),
     "pair_loss_sigmoid_workspace_bytes": (c_size_t, [c_size_t, c_size_t, c_size_t]),
+    "pair_loss_sigmoid_matryoshka_fwd_bwd": (c_int, [ctypes.POINTER(PairLossMatryoshkaArgs)]),
+    "pair_loss_sigmoid_matryoshka_workspace_bytes": (c_size_t, [c_size_t, c_size_t, c_size_t]),
     "pair_loss_sigmoid_scores_fwd_bwd": (c_int, [ctypes.POINTER(PairLossSigmoidScoresArgs)]),
     "pair_loss_sigmoid_scores_workspace_bytes": (c_size_t, [c_size_t, c_size_t]),
     "pair_loss_scores_fwd_bwd": (c_int, [ctypes.POINTER(PairLossScoresArgs)]),
@@ -254,6 +264,48 @@ def pair_loss_sigmoid_fwd_bwd(embeddings, inverse_temperature, bias, attract, re
         device_status=_ptr(st), stream=_stream(stream))
     raise_for(lib.pair_loss_sigmoid_fwd_bwd(ctypes.byref(args)), "pair_loss_sigmoid_fwd_bwd")
     return dict(loss=loss, d_embeddings=de, d_inverse_temperature=dt, d_bias=db, device_status=st)
+
+
+def pair_loss_sigmoid_matryoshka_workspace_bytes(count, width, edges):
+    return int(lib.pair_loss_sigmoid_matryoshka_workspace_bytes(count, width, edges))
+
+
+def pair_loss_sigmoid_matryoshka_fwd_bwd(embeddings, prefix_widths, inverse_temperature, bias, attract, repel=None,
+                                         ignore=None, negatives_named=False, ambient_weight=1.0, out=None,
+                                         workspace=None, device_status=None, stream=None):
+    """The pooled sigmoid pair loss summed over the normalised prefixes `prefix_widths` of bf16 embeddings
+    [N, ld] (first `width` = embeddings.shape[1] columns unless `out['width']` narrows it).  Returns
+    dict(loss, d_embeddings, d_inverse_temperature, d_bias, prefix_loss, device_status) of device tensors."""
+    _check_cuda(embeddings, "embeddings", torch.bfloat16)
+    _check_cuda(inverse_temperature, "inverse_temperature", torch.float32)
+    _check_cuda(bias, "bias", torch.float32)
+    n, ld = embeddings.shape
+    width = (out or {}).get("width", ld)
+    dev = embeddings.device
+    out = dict(out or {})
+    widths = (c_size_t * len(prefix_widths))(*[int(p) for p in prefix_widths])
+    loss = out.get("loss") if out.get("loss") is not None else torch.empty(1, device=dev)
+    de = out.get("d_embeddings") if out.get("d_embeddings") is not None else torch.empty(n, width, device=dev)
+    dt = out.get("d_inverse_temperature") if out.get("d_inverse_temperature") is not None else torch.empty(1, device=dev)
+    db = out.get("d_bias") if out.get("d_bias") is not None else torch.empty(1, device=dev)
+    pl = out.get("prefix_loss") if out.get("prefix_loss") is not None else torch.empty(max(1, len(prefix_widths)),
+                                                                                         device=dev)
+    st = device_status if device_status is not None else torch.zeros(1, dtype=torch.int32, device=dev)
+    A, R, I = _edges(attract, n), _edges(repel, n), _edges(ignore, n)
+    total = A.edges + R.edges + I.edges
+    need = pair_loss_sigmoid_matryoshka_workspace_bytes(n, width, total)
+    ws = workspace if workspace is not None else _ws(need, dev)
+    base = PairLossSigmoidArgs(
+        count=n, width=width, ld=embeddings.stride(0), embeddings=_ptr(embeddings),
+        inverse_temperature=_ptr(inverse_temperature), bias=_ptr(bias),
+        relations=Relations(A, R, I, int(bool(negatives_named)), float(ambient_weight)),
+        loss=_ptr(loss), d_embeddings=_ptr(de), ld_d_embeddings=de.stride(0),
+        d_inverse_temperature=_ptr(dt), d_bias=_ptr(db), workspace=_ptr(ws), workspace_bytes=ws.numel(),
+        device_status=_ptr(st), stream=_stream(stream))
+    args = PairLossMatryoshkaArgs(base=base, prefix_widths=ctypes.cast(widths, c_void_p),
+                                  prefix_count=len(prefix_widths), prefix_loss=_ptr(pl))
+    raise_for(lib.pair_loss_sigmoid_matryoshka_fwd_bwd(ctypes.byref(args)), "pair_loss_sigmoid_matryoshka_fwd_bwd")
+    return dict(loss=loss, d_embeddings=de, d_inverse_temperature=dt, d_bias=db, prefix_loss=pl, device_status=st)
 
 
 def pair_loss_sigmoid_scores_workspace_bytes(rows, cols):

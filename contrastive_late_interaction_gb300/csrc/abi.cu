@@ -95,8 +95,14 @@ size_t pair_loss_sigmoid_workspace_bytes(size_t count, size_t width, size_t edge
     return carve_pooled_workspace(nullptr, count, width, edges).bytes;
 }
 
-cli_status_t pair_loss_sigmoid_fwd_bwd(const cli_pair_loss_sigmoid_t *a) {
-    if (!a) return CLI_INVALID_ARGUMENT;
+}  // extern "C"
+
+namespace cli {
+namespace {
+
+// Host checks of a pooled call that need no workspace layout; `edges` receives
+// the total size of the three edge sets.
+cli_status_t pooled_checks(const cli_pair_loss_sigmoid_t *a, size_t &edges) {
     const cli_relations_t &rel = a->relations;
     if (!a->embeddings || !a->inverse_temperature || !a->bias || !a->loss || !a->d_embeddings ||
         !a->d_inverse_temperature || !a->d_bias || !a->device_status || !a->workspace)
@@ -111,12 +117,15 @@ cli_status_t pair_loss_sigmoid_fwd_bwd(const cli_pair_loss_sigmoid_t *a) {
     // "a contrastive step naming no attract edge" is refused (Training, uform_trainer_step).
     if (!rel.attract.offsets || rel.attract.edges == 0) return CLI_INVALID_ARGUMENT;
     if (!(rel.ambient_weight >= 0.0f) || std::isinf(rel.ambient_weight)) return CLI_INVALID_ARGUMENT;
-    const size_t edges = rel.attract.edges + (rel.repel.offsets ? rel.repel.edges : 0) +
-                         (rel.ignore.offsets ? rel.ignore.edges : 0);
+    edges = rel.attract.edges + (rel.repel.offsets ? rel.repel.edges : 0) + (rel.ignore.offsets ? rel.ignore.edges : 0);
     if (edges >= (1ull << 30)) return CLI_UNSUPPORTED;
-    const PooledWorkspace ws = carve_pooled_workspace(a->workspace, a->count, a->width, edges);
-    if (a->workspace_bytes < ws.bytes) return CLI_INVALID_ARGUMENT;
+    return CLI_OK;
+}
 
+// True when an output of a pooled call (the workspace taken as ws_bytes, plus
+// an optional extra output range) overlaps an input or another output.
+bool pooled_overlap(const cli_pair_loss_sigmoid_t *a, size_t ws_bytes, Range extra) {
+    const cli_relations_t &rel = a->relations;
     const size_t n = a->count;
     const Range inputs[] = {
         range_of(a->embeddings, ((n - 1) * a->ld + a->width) * 2),
@@ -136,11 +145,53 @@ cli_status_t pair_loss_sigmoid_fwd_bwd(const cli_pair_loss_sigmoid_t *a) {
         range_of(a->d_embeddings, ((n - 1) * a->ld_d_embeddings + a->width) * 4),
         range_of(a->d_inverse_temperature, 4),
         range_of(a->d_bias, 4),
-        range_of(a->workspace, ws.bytes),
+        range_of(a->workspace, ws_bytes),
         range_of(a->device_status, 4),
+        extra,
     };
-    if (any_overlap(inputs, sizeof(inputs) / sizeof(inputs[0]), outputs, sizeof(outputs) / sizeof(outputs[0])))
-        return CLI_INVALID_ARGUMENT;
+    return any_overlap(inputs, sizeof(inputs) / sizeof(inputs[0]), outputs, sizeof(outputs) / sizeof(outputs[0]));
+}
+
+// The pooled kernel's launch record for embeddings `e` of width `width`
+// (written dE d_e with row stride ld_de) and scalar outputs loss, dt, db.
+PooledLaunch pooled_launch_record(const cli_pair_loss_sigmoid_t *a, const PooledWorkspace &ws, int width, float *d_e,
+                                  long long ld_de, float *loss, float *dt, float *db, int sms) {
+    PooledLaunch L;
+    L.n = static_cast<int>(a->count);
+    L.width = width;
+    L.t_ptr = a->inverse_temperature;
+    L.b_ptr = a->bias;
+    L.ambient = a->relations.ambient_weight;
+    L.named = a->relations.negatives_named ? 1 : 0;
+    L.rel_off = ws.rel_off;
+    L.rel = ws.rel;
+    L.d_e = d_e;
+    L.ld_de = ld_de;
+    L.partials = ws.partials;
+    L.sums = ws.sums;
+    L.loss = loss;
+    L.dt = dt;
+    L.db = db;
+    L.status = a->device_status;
+    L.sm_count = sms;
+    return L;
+}
+
+}  // namespace
+}  // namespace cli
+
+extern "C" {
+
+cli_status_t pair_loss_sigmoid_fwd_bwd(const cli_pair_loss_sigmoid_t *a) {
+    if (!a) return CLI_INVALID_ARGUMENT;
+    const cli_relations_t &rel = a->relations;
+    size_t edges = 0;
+    const cli_status_t st = pooled_checks(a, edges);
+    if (st != CLI_OK) return st;
+    const PooledWorkspace ws = carve_pooled_workspace(a->workspace, a->count, a->width, edges);
+    if (a->workspace_bytes < ws.bytes) return CLI_INVALID_ARGUMENT;
+    if (pooled_overlap(a, ws.bytes, Range{0, 0})) return CLI_INVALID_ARGUMENT;
+    const size_t n = a->count;
 
     const int sms = sm_count();
     if (sms <= 0) return CLI_DEVICE;
@@ -155,25 +206,71 @@ cli_status_t pair_loss_sigmoid_fwd_bwd(const cli_pair_loss_sigmoid_t *a) {
         return CLI_DEVICE;
     if (cudaMemset2DAsync(a->d_embeddings, a->ld_d_embeddings * 4, 0, a->width * 4, n, stream) != cudaSuccess)
         return CLI_DEVICE;
-    PooledLaunch L;
-    L.n = static_cast<int>(n);
-    L.width = static_cast<int>(a->width);
-    L.t_ptr = a->inverse_temperature;
-    L.b_ptr = a->bias;
-    L.ambient = rel.ambient_weight;
-    L.named = rel.negatives_named ? 1 : 0;
-    L.rel_off = ws.rel_off;
-    L.rel = ws.rel;
-    L.d_e = a->d_embeddings;
-    L.ld_de = static_cast<long long>(a->ld_d_embeddings);
-    L.partials = ws.partials;
-    L.sums = ws.sums;
-    L.loss = a->loss;
-    L.dt = a->d_inverse_temperature;
-    L.db = a->d_bias;
-    L.status = a->device_status;
-    L.sm_count = sms;
+    const PooledLaunch L = pooled_launch_record(a, ws, static_cast<int>(a->width), a->d_embeddings,
+                                                static_cast<long long>(a->ld_d_embeddings), a->loss,
+                                                a->d_inverse_temperature, a->d_bias, sms);
     if (launch_pooled_fused(tmap, L, stream) != cudaSuccess) return CLI_DEVICE;
+    return CLI_OK;
+}
+
+// ----------------------------------------------------------------------------
+// Matryoshka prefixes of the pooled sigmoid pair loss
+// ----------------------------------------------------------------------------
+
+size_t pair_loss_sigmoid_matryoshka_workspace_bytes(size_t count, size_t width, size_t edges) {
+    return carve_matryoshka_workspace(nullptr, count, width, edges).bytes;
+}
+
+cli_status_t pair_loss_sigmoid_matryoshka_fwd_bwd(const cli_pair_loss_matryoshka_t *m) {
+    if (!m) return CLI_INVALID_ARGUMENT;
+    const cli_pair_loss_sigmoid_t *a = &m->base;
+    const cli_relations_t &rel = a->relations;
+    size_t edges = 0;
+    const cli_status_t st = pooled_checks(a, edges);
+    if (st != CLI_OK) return st;
+    if (!m->prefix_widths) return CLI_INVALID_ARGUMENT;
+    if (m->prefix_count == 0 || m->prefix_count > CLI_MATRYOSHKA_MAX_PREFIXES) return CLI_SHAPE_MISMATCH;
+    for (size_t k = 0; k < m->prefix_count; ++k) {
+        const size_t p = m->prefix_widths[k];
+        if (p == 0 || p % 8 != 0 || p > a->width) return CLI_SHAPE_MISMATCH;
+        if (k > 0 && p <= m->prefix_widths[k - 1]) return CLI_SHAPE_MISMATCH;
+    }
+    if (m->prefix_loss && !aligned(m->prefix_loss, 4)) return CLI_INVALID_ARGUMENT;
+    const MatryoshkaWorkspace ws = carve_matryoshka_workspace(a->workspace, a->count, a->width, edges);
+    if (a->workspace_bytes < ws.bytes) return CLI_INVALID_ARGUMENT;
+    if (pooled_overlap(a, ws.bytes, range_of(m->prefix_loss, m->prefix_loss ? m->prefix_count * 4 : 0)))
+        return CLI_INVALID_ARGUMENT;
+
+    const int sms = sm_count();
+    if (sms <= 0) return CLI_DEVICE;
+    const size_t n = a->count;
+    const int ni = static_cast<int>(n);
+    cudaStream_t stream = static_cast<cudaStream_t>(a->stream);
+    const uint16_t *e = static_cast<const uint16_t *>(static_cast<const void *>(a->embeddings));
+    const long long ld = static_cast<long long>(a->ld);
+    if (cudaMemsetAsync(a->device_status, 0, sizeof(int32_t), stream) != cudaSuccess) return CLI_DEVICE;
+    const EdgeSet sets[3] = {to_set(rel.attract), to_set(rel.repel), to_set(rel.ignore)};
+    if (launch_relation_prep(sets, ni, rel.negatives_named, rel.ambient_weight, ws.pooled, a->device_status, stream) !=
+        cudaSuccess)
+        return CLI_DEVICE;
+    if (cudaMemset2DAsync(a->d_embeddings, a->ld_d_embeddings * 4, 0, a->width * 4, n, stream) != cudaSuccess)
+        return CLI_DEVICE;
+    for (size_t k = 0; k < m->prefix_count; ++k) {
+        const int p = static_cast<int>(m->prefix_widths[k]);
+        CUtensorMap tmap;
+        if (!encode_bf16_rows(&tmap, ws.u, static_cast<uint64_t>(p), n, static_cast<uint64_t>(p))) return CLI_DEVICE;
+        if (launch_prefix_normalize(e, ld, ni, p, ws, a->device_status, stream) != cudaSuccess) return CLI_DEVICE;
+        if (cudaMemsetAsync(ws.de_p, 0, n * static_cast<size_t>(p) * 4, stream) != cudaSuccess) return CLI_DEVICE;
+        float *sc = ws.scalars + 3 * k;
+        const PooledLaunch L = pooled_launch_record(a, ws.pooled, p, ws.de_p, p, sc, sc + 1, sc + 2, sms);
+        if (launch_pooled_fused(tmap, L, stream) != cudaSuccess) return CLI_DEVICE;
+        if (launch_prefix_backprop(e, ld, ni, p, ws, a->d_embeddings, static_cast<long long>(a->ld_d_embeddings),
+                                   a->device_status, stream) != cudaSuccess)
+            return CLI_DEVICE;
+    }
+    if (launch_matryoshka_finish(ws, static_cast<int>(m->prefix_count), a->loss, a->d_inverse_temperature, a->d_bias,
+                                 m->prefix_loss, a->device_status, stream) != cudaSuccess)
+        return CLI_DEVICE;
     return CLI_OK;
 }
 

@@ -70,6 +70,26 @@ size_t pooled_fused_smem_bytes();
 long long pooled_partial_slots(int n);
 int pooled_finish_blocks();
 
+// Matryoshka prefixes: the pooled workspace, then a bf16 copy of the
+// normalised prefix rows, their inverse norms, the prefix's dE and the
+// per-prefix (loss, dt, db).
+constexpr int kMaxMatryoshkaPrefixes = 8;
+struct MatryoshkaWorkspace {
+    PooledWorkspace pooled;
+    uint16_t *u;           // [n][width] bf16 (a prefix of width p uses row stride p)
+    float *inv_norm;       // [n]
+    float *de_p;           // [n][width] fp32 (row stride p)
+    float *scalars;        // [kMaxMatryoshkaPrefixes][3]
+    size_t bytes;
+};
+MatryoshkaWorkspace carve_matryoshka_workspace(void *base, size_t n, size_t width, size_t edges_total);
+cudaError_t launch_prefix_normalize(const uint16_t *e, long long ld, int n, int p, const MatryoshkaWorkspace &ws,
+                                    const int32_t *status, cudaStream_t stream);
+cudaError_t launch_prefix_backprop(const uint16_t *e, long long ld, int n, int p, const MatryoshkaWorkspace &ws,
+                                   float *de, long long ld_de, const int32_t *status, cudaStream_t stream);
+cudaError_t launch_matryoshka_finish(const MatryoshkaWorkspace &ws, int count, float *loss, float *dt, float *db,
+                                     float *prefix_loss, const int32_t *status, cudaStream_t stream);
+
 // Score-matrix loss.
 struct ScoreLossLaunch {
     int rows, cols;

@@ -144,6 +144,42 @@ cli_status_t pair_loss_sigmoid_fwd_bwd(const cli_pair_loss_sigmoid_t *args);
 size_t pair_loss_sigmoid_workspace_bytes(size_t count, size_t width, size_t edges);
 
 /*
+ * pair_loss_sigmoid_matryoshka_fwd_bwd -- the pooled sigmoid pair loss over
+ * nested prefixes of the embeddings ("Training", `uform_contrastive_t`,
+ * `matryoshka_dimensions`: prefix widths strictly ascending, each a multiple
+ * of 8, at most 8, every one scored; "UForm", section "Matryoshka-Like
+ * Multi-Scale Embedders": each prefix is trained under the SigLIP loss on
+ * cosine similarities):
+ *     u_p,i = e_i[:p] / |e_i[:p]|,   L = sum_p L_sigmoid(u_p),
+ * with one (t, b) for every prefix; dE, dt and db are the gradients of that
+ * sum.  The library normalises each prefix (the caller's rows need not be unit
+ * vectors), scores a bf16 copy of it (nearest-even rounding) and passes the
+ * gradient through the normalisation; a prefix of zero norm scores the zero
+ * vector and passes no gradient.  The full width is scored only if listed.
+ *
+ *   base            every field as in cli_pair_loss_sigmoid_t; `base.workspace`
+ *                   must hold pair_loss_sigmoid_matryoshka_workspace_bytes
+ *   prefix_widths   host array of prefix_count widths, read before the call
+ *                   returns; 1 <= prefix_count <= CLI_MATRYOSHKA_MAX_PREFIXES,
+ *                   strictly ascending, multiples of 8, at most base.width
+ *                   (CLI_SHAPE_MISMATCH otherwise)
+ *   prefix_loss     device fp32 [prefix_count] (written), each prefix's loss;
+ *                   may be NULL
+ */
+#define CLI_MATRYOSHKA_MAX_PREFIXES 8
+typedef struct {
+    cli_pair_loss_sigmoid_t base;
+    const size_t *prefix_widths;
+    size_t prefix_count;
+    float *prefix_loss;
+} cli_pair_loss_matryoshka_t;
+
+cli_status_t pair_loss_sigmoid_matryoshka_fwd_bwd(const cli_pair_loss_matryoshka_t *args);
+
+/* Workspace bytes for pair_loss_sigmoid_matryoshka_fwd_bwd (any prefix list). */
+size_t pair_loss_sigmoid_matryoshka_workspace_bytes(size_t count, size_t width, size_t edges);
+
+/*
  * pair_loss_sigmoid_scores_fwd_bwd -- the same sigmoid pair loss over a given
  * rows x cols score matrix S (e.g. hard MaxSim scores of queries against
  * documents, "UForm", section "ColBERT-Style Late-Interaction Rerankers":

@@ -162,3 +162,29 @@ def test_score_loss_host_checks(b):
     assert f(cols=32, ld=32, ld_d_scores=32, sides=A * 12) == b.CLI_SHAPE_MISMATCH   # sides need a square matrix
     assert f(d_scores=A * 1) == b.CLI_INVALID_ARGUMENT
     assert f(workspace_bytes=0) == b.CLI_INVALID_ARGUMENT
+
+
+def test_matryoshka_host_checks(b):
+    n, w = 1024, 512
+    ws = b.pair_loss_sigmoid_matryoshka_workspace_bytes(n, w, 2048)
+    assert ws > b.pair_loss_sigmoid_workspace_bytes(n, w, 2048)
+
+    def f(widths, count=None, prefix_loss=A * 12, **over):
+        arr = (ctypes.c_size_t * max(1, len(widths)))(*widths) if widths is not None else None
+        args = b.PairLossMatryoshkaArgs(base=pooled_args(b, **{"workspace_bytes": ws, **over}),
+                                        prefix_widths=ctypes.cast(arr, ctypes.c_void_p) if arr is not None else None,
+                                        prefix_count=len(widths) if count is None else count,
+                                        prefix_loss=prefix_loss)
+        return b.lib.pair_loss_sigmoid_matryoshka_fwd_bwd(ctypes.byref(args))
+
+    assert b.lib.pair_loss_sigmoid_matryoshka_fwd_bwd(None) == b.CLI_INVALID_ARGUMENT
+    assert f(None, count=1) == b.CLI_INVALID_ARGUMENT                     # no prefix list
+    assert f([64], count=0) == b.CLI_SHAPE_MISMATCH
+    assert f([8 * (k + 1) for k in range(9)]) == b.CLI_SHAPE_MISMATCH    # more than eight prefixes
+    assert f([64, 64]) == b.CLI_SHAPE_MISMATCH                           # not strictly ascending
+    assert f([128, 64]) == b.CLI_SHAPE_MISMATCH
+    assert f([60, 128]) == b.CLI_SHAPE_MISMATCH                          # not a multiple of 8
+    assert f([64, 520]) == b.CLI_SHAPE_MISMATCH                          # past the width
+    assert f([64], workspace_bytes=b.pair_loss_sigmoid_workspace_bytes(n, w, 2048)) == b.CLI_INVALID_ARGUMENT
+    assert f([64], prefix_loss=A * 1) == b.CLI_INVALID_ARGUMENT          # an output inside the embeddings
+    assert f([64], embeddings=None) == b.CLI_INVALID_ARGUMENT            # the pooled checks still apply
