@@ -42,7 +42,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["joint", "pooled2", "maxsim3", "pooled4"], default="joint")
+    ap.add_argument("--workload", choices=["joint", "pooled2", "maxsim3", "pooled4", "matryoshka5"], default="joint")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work budget of the oracle baseline")
@@ -57,18 +57,22 @@ def make_workload(name: str, seed: int):
     from contrastive_late_interaction_gb300 import synth
     if name == "joint":
         j = synth.joint_config5(seed)
-        return dict(pooled=j.pooled, maxsim=j.maxsim, joint=j)
+        return dict(pooled=j.pooled, maxsim=j.maxsim, joint=j, prefixes=None)
     if name == "pooled2":
-        return dict(pooled=synth.pooled_config2(seed), maxsim=None, joint=None)
+        return dict(pooled=synth.pooled_config2(seed), maxsim=None, joint=None, prefixes=None)
     if name == "pooled4":
-        return dict(pooled=synth.pooled_config4(seed), maxsim=None, joint=None)
+        return dict(pooled=synth.pooled_config4(seed), maxsim=None, joint=None, prefixes=None)
     if name == "maxsim3":
-        return dict(pooled=None, maxsim=synth.maxsim_config3(seed), joint=None)
+        return dict(pooled=None, maxsim=synth.maxsim_config3(seed), joint=None, prefixes=None)
+    if name == "matryoshka5":
+        # the joint step's pooled batch scored at the nested prefixes {64, 128, 256, 512}
+        return dict(pooled=synth.joint_config5(seed).pooled, maxsim=None, joint=None, prefixes=[64, 128, 256, 512])
     raise ValueError(name)
 
 
-def pooled_flops(p):
-    return 3.0 * p.count * p.count * p.width
+def pooled_flops(p, prefixes=None):
+    """3 N^2 D per scored width (S by symmetry plus the two gradient contractions)."""
+    return sum(3.0 * p.count * p.count * w for w in (prefixes or [p.width]))
 
 
 def maxsim_fwd_flops(m):
@@ -82,12 +86,15 @@ def maxsim_bwd_flops(m):
 def describe(name, w):
     cfg = {"workload": {"joint": "joint contrastive step (config 5)", "pooled2": "pooled sigmoid loss (config 2)",
                         "pooled4": "large pooled sigmoid loss (config 4)",
-                        "maxsim3": "MaxSim fwd+bwd (config 3)"}[name]}
+                        "maxsim3": "MaxSim fwd+bwd (config 3)",
+                        "matryoshka5": "Matryoshka prefixes of the pooled sigmoid loss (config 5 pooled batch)"}[name]}
     p, m = w["pooled"], w["maxsim"]
     if p is not None:
         cfg["pooled"] = {"N": p.count, "D": p.width, "t": p.t, "b": p.b,
                          "attract_edges": int(p.attract.ids.size), "ignore_edges": int(p.ignore.ids.size),
                          "negatives": "named" if p.negatives_named else "ambient"}
+        if w.get("prefixes"):
+            cfg["pooled"]["prefixes"] = list(w["prefixes"])
     if m is not None:
         cfg["maxsim"] = {"queries": m.nq, "documents": m.nd, "D": m.width, "query_rows": int(m.q_offsets[-1]),
                          "document_rows": int(m.d_offsets[-1]), "form": "mean" if m.mean else "sum"}
@@ -110,6 +117,7 @@ class Step:
         self.cli, self.torch, self.stream, self.dev = cli, torch, stream, device
         self.w = w
         self.p, self.m, self.j = w["pooled"], w["maxsim"], w["joint"]
+        self.prefixes = w.get("prefixes")
         self.host = {}      # pinned host copies for the end-to-end measurement
         self.dev_in = {}
         with torch.cuda.stream(stream):
@@ -141,10 +149,13 @@ class Step:
             self.ign = ((self._pin("ign_off", p.ignore.offsets), self._pin("ign_ids", p.ignore.ids))
                         if p.ignore.ids.size else None)
             edges = int(p.attract.ids.size + p.ignore.ids.size)
-            self.p_ws = torch.empty(cli.pair_loss_sigmoid_workspace_bytes(p.count, p.width, edges),
-                                    dtype=torch.uint8, device=self.dev)
+            sizer = (cli.pair_loss_sigmoid_matryoshka_workspace_bytes if self.prefixes else
+                     cli.pair_loss_sigmoid_workspace_bytes)
+            self.p_ws = torch.empty(sizer(p.count, p.width, edges), dtype=torch.uint8, device=self.dev)
             self.p_out = dict(loss=torch.empty(1, **f32), d_embeddings=torch.empty(p.count, p.width, **f32),
                               d_inverse_temperature=torch.empty(1, **f32), d_bias=torch.empty(1, **f32))
+            if self.prefixes:
+                self.p_out["prefix_loss"] = torch.empty(len(self.prefixes), **f32)
             self.p_st = torch.zeros(1, dtype=torch.int32, device=self.dev)
         if self.m is not None:
             m = self.m
@@ -182,7 +193,10 @@ class Step:
         if self.p is not None:
             n += 1 + (1 if self.ign is not None else 0)   # edge validation, one per edge set given
             n += 1 + 3 + 1 + 1 + 1 + 1 + 1                # in-degree, 3 scans, fill, sort, count, scan, emit
-            n += 2                                        # fused tile kernel, final reduction
+            if self.prefixes:                             # per prefix: normalise, fused, 2 reductions, gradient
+                n += 5 * len(self.prefixes) + 1           # and the sum over prefixes
+            else:
+                n += 3                                    # fused block kernel, two-level final reduction
         if self.m is not None:
             n += 2 + 1 + 1 + 1                            # 2 tape validations, schedule, forward, query sums
             n += 2 + 1 + 1 + 1                            # 2 tape validations, row->query map, dQ, dD
@@ -201,8 +215,13 @@ class Step:
         with self.torch.cuda.stream(self.stream):
             if self.p is not None:
                 rec("pooled", 0)
-                cli.pair_loss_sigmoid_fwd_bwd(self.e, self.t, self.b, self.att, None, self.ign, out=self.p_out,
-                                              workspace=self.p_ws, device_status=self.p_st, stream=self.stream)
+                if self.prefixes:
+                    cli.pair_loss_sigmoid_matryoshka_fwd_bwd(self.e, self.prefixes, self.t, self.b, self.att, None,
+                                                             self.ign, out=self.p_out, workspace=self.p_ws,
+                                                             device_status=self.p_st, stream=self.stream)
+                else:
+                    cli.pair_loss_sigmoid_fwd_bwd(self.e, self.t, self.b, self.att, None, self.ign, out=self.p_out,
+                                                  workspace=self.p_ws, device_status=self.p_st, stream=self.stream)
                 rec("pooled", 1)
             if self.m is not None:
                 rec("maxsim_fwd", 0)
@@ -350,20 +369,28 @@ def oracle_sample(w, budget_s: float, threads: int):
     flops = secs = 0.0
     desc = []
     if p is not None:
-        e = p.e_rounded
+        pre = w.get("prefixes")
+        if pre:   # the oracle's normalised, bf16-rounded prefixes, as its Matryoshka function scores them
+            ee = []
+            for q in pre:
+                x = p.e_rounded[:, :q]
+                ee.append(oracle.round_bf16(x / np.linalg.norm(x, axis=1, keepdims=True)))
+        else:
+            ee = [p.e_rounded]
         r = 8
         while True:
             rows = np.arange(r)
             t0 = time.perf_counter()
-            oracle.pair_loss_sigmoid(e, p.t, p.b, p.attract, ignore=p.ignore if p.ignore.ids.size else None,
-                                     rows=rows, threads=threads)
+            for e in ee:
+                oracle.pair_loss_sigmoid(e, p.t, p.b, p.attract, ignore=p.ignore if p.ignore.ids.size else None,
+                                         rows=rows, threads=threads)
             dt = time.perf_counter() - t0
             if dt > budget_s / parts / 4 or r >= p.count:
                 break
             r = min(p.count, max(r * 2, int(r * (budget_s / parts) / max(dt, 1e-3) / 2)))
-        flops += 3.0 * p.count * p.width * r
+        flops += sum(3.0 * p.count * e.shape[1] * r for e in ee)
         secs += dt
-        desc.append(f"pooled: {r} of {p.count} anchors")
+        desc.append(f"pooled: {r} of {p.count} anchors" + (f" at each of the prefixes {pre}" if pre else ""))
     if m is not None:
         rng = np.random.default_rng(0)
         k = 16
@@ -491,16 +518,17 @@ def main():
     step_ms = [s.elapsed_time(e) for s, e in st_ev]
     part_ms = {n: [ev[k][n][0].elapsed_time(ev[k][n][1]) for k in range(args.steps)] for n in names}
     p, m = step.p, step.m
-    flops = (pooled_flops(p) if p is not None else 0.0) + \
+    pre = w.get("prefixes")
+    flops = (pooled_flops(p, pre) if p is not None else 0.0) + \
             ((maxsim_fwd_flops(m) + maxsim_bwd_flops(m)) if m is not None else 0.0)
     ms, value = aggregate(pg, world, flops, statistics.mean(step_ms), device)
     burst, sustained, hbm, peak_src = peaks()
     parts = {}
     if p is not None:
         pm = statistics.mean(part_ms["pooled"])
-        parts["pair_loss"] = {"ms": pm, "pairs_per_s": p.count * (p.count - 1) / (pm * 1e-3),
-                              "tflops": pooled_flops(p) / (pm * 1e-3) / 1e12,
-                              "frac_of_peak": pooled_flops(p) / (pm * 1e-3) / 1e12 / sustained}
+        parts["pair_loss"] = {"ms": pm, "pairs_per_s": len(pre or [0]) * p.count * (p.count - 1) / (pm * 1e-3),
+                              "tflops": pooled_flops(p, pre) / (pm * 1e-3) / 1e12,
+                              "frac_of_peak": pooled_flops(p, pre) / (pm * 1e-3) / 1e12 / sustained}
     if m is not None:
         fm, bm = statistics.mean(part_ms["maxsim_fwd"]), statistics.mean(part_ms["maxsim_bwd"])
         tf = (maxsim_fwd_flops(m) + maxsim_bwd_flops(m)) / ((fm + bm) * 1e-3) / 1e12
@@ -522,11 +550,12 @@ def main():
                     "algorithmic_per_launch": maxsim_fwd_flops(m)}
     else:
         pm = statistics.mean(part_ms["pooled"])
-        achieved = pooled_flops(p) / (pm * 1e-3) / 1e12
-        roofline = {"kernel": "pooled fused tile kernel (pair_loss_sigmoid_fwd_bwd call)", "bound": "tensor",
+        achieved = pooled_flops(p, pre) / (pm * 1e-3) / 1e12
+        call = "pair_loss_sigmoid_matryoshka_fwd_bwd" if pre else "pair_loss_sigmoid_fwd_bwd"
+        roofline = {"kernel": f"pooled fused block kernel ({call} call)", "bound": "tensor",
                     "achieved": achieved, "peak": sustained, "unit": "TFLOP/s", "frac": achieved / sustained,
                     "peak_source": f"{peak_src} bf16 sustained", "traffic": None,
-                    "algorithmic_per_launch": pooled_flops(p)}
+                    "algorithmic_per_launch": pooled_flops(p, pre)}
 
     # end to end through the C ABI with host buffers: inputs copied in, losses read back, every step
     e2e = None
