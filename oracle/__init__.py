@@ -140,6 +140,63 @@ def pair_loss_sigmoid(e, t, b, attract=None, repel=None, ignore=None, negatives_
     return dict(loss=out[0], dt=out[1], db=out[2], de=de, row_loss=row_loss)
 
 
+def _dense_relations(n, attract, repel, ignore, negatives_named, ambient_weight):
+    """(Y, W): Y[i, j] = +1 attract, -1 repel, 0 skipped; W the weight; resolved in the documented order
+    ("Training", `uform_relations_view_t`: ignore, then attract, then repel, then the negatives default;
+    `uform_negatives_t`: ambient repels at `ambient_weight`, named scores only repel edges).  The diagonal
+    is never scored."""
+    Y = np.full((n, n), 0 if negatives_named else -1, dtype=np.int8)
+    W = np.full((n, n), 0.0 if negatives_named else float(ambient_weight))
+
+    def each(edges):
+        off, ids, w = _edges(edges)
+        if off is None:
+            return
+        for i in range(n):
+            for k in range(int(off[i]), int(off[i + 1])):
+                yield i, int(ids[k]), (1.0 if w is None else float(w[k]))
+
+    for i, j, w in each(repel):
+        Y[i, j], W[i, j] = -1, w
+    for i, j, w in each(attract):
+        Y[i, j], W[i, j] = 1, w
+    for i, j, _ in each(ignore):
+        Y[i, j], W[i, j] = 0, 0.0
+    np.fill_diagonal(Y, 0)
+    W[Y == 0] = 0.0
+    return Y, W
+
+
+def pair_loss_sigmoid_groups(e, groups, t, b, attract=None, repel=None, ignore=None, negatives_named=False,
+                             ambient_weight=1.0):
+    """Pooled sigmoid pair loss with temperature groups.  Returns dict(loss, dt, db, de) with dt, db one per
+    group.
+
+    "Training", `uform_contrastive_t` (`temperature_groups`: learnable (inverse temperature, bias) pairs,
+    one per group a step's items select).  Reading: item i selects group g(i), and a cell takes its
+    anchor's pair: z_ij = t[g(i)] s_ij + b[g(i)], l_ij = w_ij softplus(-y_ij z_ij), L = (1/N) sum l_ij
+    (the SigLIP loss of "UForm", section "Matryoshka-Like Multi-Scale Embedders", per anchor).  Written out
+    densely in float64 (a second formulation beside the C oracle, which it equals with one group).
+    """
+    e = _f64(e)
+    n = e.shape[0]
+    g = np.asarray(groups, dtype=np.int64)
+    tv, bv = np.asarray(t, dtype=np.float64), np.asarray(b, dtype=np.float64)
+    Y, W = _dense_relations(n, attract, repel, ignore, negatives_named, ambient_weight)
+    S = e @ e.T
+    Z = tv[g][:, None] * S + bv[g][:, None]
+    m = -Y * Z                                    # softplus(-y z) and its derivative sigma(-y z)
+    sp = np.maximum(m, 0.0) + np.log1p(np.exp(-np.abs(m)))
+    sg = np.where(m >= 0, 1.0 / (1.0 + np.exp(-np.abs(m))), np.exp(-np.abs(m)) / (1.0 + np.exp(-np.abs(m))))
+    Gz = -W * Y * sg / n                          # dL/dz_ij
+    loss = float(np.sum(W * sp) / n)
+    dS = tv[g][:, None] * Gz
+    de = (dS + dS.T) @ e
+    dt = np.bincount(g, weights=np.sum(Gz * S, axis=1), minlength=len(tv))
+    db = np.bincount(g, weights=np.sum(Gz, axis=1), minlength=len(tv))
+    return dict(loss=loss, dt=dt, db=db, de=de)
+
+
 def round_bf16(x):
     """Nearest-even rounding of float64 values to bfloat16 (through float32), returned as float64.
     The device scores bf16 copies of the normalised prefixes; the oracle scores the same values."""
