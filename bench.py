@@ -42,7 +42,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["joint", "pooled2", "maxsim3", "pooled4", "matryoshka5"], default="joint")
+    ap.add_argument("--workload", choices=["joint", "pooled2", "maxsim3", "pooled4", "matryoshka5", "groups5"], default="joint")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work budget of the oracle baseline")
@@ -67,6 +67,12 @@ def make_workload(name: str, seed: int):
     if name == "matryoshka5":
         # the joint step's pooled batch scored at the nested prefixes {64, 128, 256, 512}
         return dict(pooled=synth.joint_config5(seed).pooled, maxsim=None, joint=None, prefixes=[64, 128, 256, 512])
+    if name == "groups5":
+        # the joint step's pooled batch with four temperature groups drawn uniformly per item
+        p = synth.joint_config5(seed).pooled
+        g = synth.uniform_int(seed, synth.STREAM_GROUPS, p.count, 0, 3).astype(np.int32)
+        return dict(pooled=p, maxsim=None, joint=None, prefixes=None,
+                    groups=(g, np.array([10.0, 8.0, 12.0, 6.0], np.float32), np.array([-10.0, -8.0, -12.0, -6.0], np.float32)))
     raise ValueError(name)
 
 
@@ -87,7 +93,8 @@ def describe(name, w):
     cfg = {"workload": {"joint": "joint contrastive step (config 5)", "pooled2": "pooled sigmoid loss (config 2)",
                         "pooled4": "large pooled sigmoid loss (config 4)",
                         "maxsim3": "MaxSim fwd+bwd (config 3)",
-                        "matryoshka5": "Matryoshka prefixes of the pooled sigmoid loss (config 5 pooled batch)"}[name]}
+                        "matryoshka5": "Matryoshka prefixes of the pooled sigmoid loss (config 5 pooled batch)",
+                        "groups5": "pooled sigmoid loss with four temperature groups (config 5 pooled batch)"}[name]}
     p, m = w["pooled"], w["maxsim"]
     if p is not None:
         cfg["pooled"] = {"N": p.count, "D": p.width, "t": p.t, "b": p.b,
@@ -95,6 +102,9 @@ def describe(name, w):
                          "negatives": "named" if p.negatives_named else "ambient"}
         if w.get("prefixes"):
             cfg["pooled"]["prefixes"] = list(w["prefixes"])
+        if w.get("groups"):
+            cfg["pooled"]["groups"] = {"count": int(len(w["groups"][1])), "t": w["groups"][1].tolist(),
+                                       "b": w["groups"][2].tolist(), "selection": "uniform per item"}
     if m is not None:
         cfg["maxsim"] = {"queries": m.nq, "documents": m.nd, "D": m.width, "query_rows": int(m.q_offsets[-1]),
                          "document_rows": int(m.d_offsets[-1]), "form": "mean" if m.mean else "sum"}
@@ -118,6 +128,7 @@ class Step:
         self.w = w
         self.p, self.m, self.j = w["pooled"], w["maxsim"], w["joint"]
         self.prefixes = w.get("prefixes")
+        self.groups = w.get("groups")
         self.host = {}      # pinned host copies for the end-to-end measurement
         self.dev_in = {}
         with torch.cuda.stream(stream):
@@ -143,8 +154,13 @@ class Step:
         if self.p is not None:
             p = self.p
             self.e = self._pin("e", p.e_bf16, torch.bfloat16)
-            self.t = self._pin("t", np.array([p.t], np.float32))
-            self.b = self._pin("b", np.array([p.b], np.float32))
+            if self.groups:
+                self.grp = self._pin("groups", self.groups[0])
+                self.t = self._pin("t", self.groups[1])
+                self.b = self._pin("b", self.groups[2])
+            else:
+                self.t = self._pin("t", np.array([p.t], np.float32))
+                self.b = self._pin("b", np.array([p.b], np.float32))
             self.att = (self._pin("att_off", p.attract.offsets), self._pin("att_ids", p.attract.ids))
             self.ign = ((self._pin("ign_off", p.ignore.offsets), self._pin("ign_ids", p.ignore.ids))
                         if p.ignore.ids.size else None)
@@ -152,8 +168,9 @@ class Step:
             sizer = (cli.pair_loss_sigmoid_matryoshka_workspace_bytes if self.prefixes else
                      cli.pair_loss_sigmoid_workspace_bytes)
             self.p_ws = torch.empty(sizer(p.count, p.width, edges), dtype=torch.uint8, device=self.dev)
+            ng = len(self.groups[1]) if self.groups else 1
             self.p_out = dict(loss=torch.empty(1, **f32), d_embeddings=torch.empty(p.count, p.width, **f32),
-                              d_inverse_temperature=torch.empty(1, **f32), d_bias=torch.empty(1, **f32))
+                              d_inverse_temperature=torch.empty(ng, **f32), d_bias=torch.empty(ng, **f32))
             if self.prefixes:
                 self.p_out["prefix_loss"] = torch.empty(len(self.prefixes), **f32)
             self.p_st = torch.zeros(1, dtype=torch.int32, device=self.dev)
@@ -193,7 +210,9 @@ class Step:
         if self.p is not None:
             n += 1 + (1 if self.ign is not None else 0)   # edge validation, one per edge set given
             n += 1 + 3 + 1 + 1 + 1 + 1 + 1                # in-degree, 3 scans, fill, sort, count, scan, emit
-            if self.prefixes:                             # per prefix: normalise, fused, 2 reductions, gradient
+            if self.groups:
+                n += 1 + 3                                # group validation, fused block kernel, final reduction
+            elif self.prefixes:                           # per prefix: normalise, fused, 2 reductions, gradient
                 n += 5 * len(self.prefixes) + 1           # and the sum over prefixes
             else:
                 n += 3                                    # fused block kernel, two-level final reduction
@@ -215,7 +234,11 @@ class Step:
         with self.torch.cuda.stream(self.stream):
             if self.p is not None:
                 rec("pooled", 0)
-                if self.prefixes:
+                if self.groups:
+                    cli.pair_loss_sigmoid_groups_fwd_bwd(self.e, self.grp, self.t, self.b, self.att, None, self.ign,
+                                                         out=self.p_out, workspace=self.p_ws, device_status=self.p_st,
+                                                         stream=self.stream)
+                elif self.prefixes:
                     cli.pair_loss_sigmoid_matryoshka_fwd_bwd(self.e, self.prefixes, self.t, self.b, self.att, None,
                                                              self.ign, out=self.p_out, workspace=self.p_ws,
                                                              device_status=self.p_st, stream=self.stream)
@@ -382,8 +405,17 @@ def oracle_sample(w, budget_s: float, threads: int):
             rows = np.arange(r)
             t0 = time.perf_counter()
             for e in ee:
-                oracle.pair_loss_sigmoid(e, p.t, p.b, p.attract, ignore=p.ignore if p.ignore.ids.size else None,
-                                         rows=rows, threads=threads)
+                if w.get("groups"):   # each sampled anchor row with its group's pair
+                    g, tv, bv = w["groups"]
+                    for q in range(len(tv)):
+                        sel = rows[g[rows] == q]
+                        if sel.size:
+                            oracle.pair_loss_sigmoid(e, float(tv[q]), float(bv[q]), p.attract,
+                                                     ignore=p.ignore if p.ignore.ids.size else None, rows=sel,
+                                                     threads=threads)
+                else:
+                    oracle.pair_loss_sigmoid(e, p.t, p.b, p.attract, ignore=p.ignore if p.ignore.ids.size else None,
+                                             rows=rows, threads=threads)
             dt = time.perf_counter() - t0
             if dt > budget_s / parts / 4 or r >= p.count:
                 break
@@ -551,7 +583,8 @@ def main():
     else:
         pm = statistics.mean(part_ms["pooled"])
         achieved = pooled_flops(p, pre) / (pm * 1e-3) / 1e12
-        call = "pair_loss_sigmoid_matryoshka_fwd_bwd" if pre else "pair_loss_sigmoid_fwd_bwd"
+        call = ("pair_loss_sigmoid_groups_fwd_bwd" if w.get("groups") else
+                "pair_loss_sigmoid_matryoshka_fwd_bwd" if pre else "pair_loss_sigmoid_fwd_bwd")
         roofline = {"kernel": f"pooled fused block kernel ({call} call)", "bound": "tensor",
                     "achieved": achieved, "peak": sustained, "unit": "TFLOP/s", "frac": achieved / sustained,
                     "peak_source": f"{peak_src} bf16 sustained", "traffic": None,
@@ -562,7 +595,7 @@ def main():
     if not args.no_e2e:
         h2d = 0
         d2h = 0
-        outs_host = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in step.results()]
+        outs_host = [torch.empty(d.shape, dtype=d.dtype).pin_memory() for d in step.results()]
         for _ in range(2):
             step.upload()
             step.run()

@@ -85,6 +85,10 @@ class PairLossSigmoidArgs(ctypes.Structure):
                 ("workspace_bytes", c_size_t), ("device_status", c_void_p), ("stream", c_void_p)]
 
 
+class PairLossGroupsArgs(ctypes.Structure):
+    _fields_ = [("base", PairLossSigmoidArgs), ("groups", c_void_p), ("group_count", c_size_t)]
+
+
 class PairLossMatryoshkaArgs(ctypes.Structure):
     _fields_ = [("base", PairLossSigmoidArgs), ("prefix_widths", c_void_p), ("prefix_count", c_size_t),
                 ("prefix_loss", c_void_p)]
@@ -130,6 +134,7 @@ EXPORTS = {
     "cli_status_name": (ctypes.c_char_p, [c_int]),
     "pair_loss_sigmoid_fwd_bwd": (c_int, [ctypes.POINTER(PairLossSigmoidArgs)]),
     "pair_loss_sigmoid_workspace_bytes": (c_size_t, [c_size_t, c_size_t, c_size_t]),
+    "pair_loss_sigmoid_groups_fwd_bwd": (c_int, [ctypes.POINTER(PairLossGroupsArgs)]),
     "pair_loss_sigmoid_matryoshka_fwd_bwd": (c_int, [ctypes.POINTER(PairLossMatryoshkaArgs)]),
     "pair_loss_sigmoid_matryoshka_workspace_bytes": (c_size_t, [c_size_t, c_size_t, c_size_t]),
     "pair_loss_sigmoid_scores_fwd_bwd": (c_int, [ctypes.POINTER(PairLossSigmoidScoresArgs)]),
@@ -263,6 +268,44 @@ def pair_loss_sigmoid_fwd_bwd(embeddings, inverse_temperature, bias, attract, re
         d_inverse_temperature=_ptr(dt), d_bias=_ptr(db), workspace=_ptr(ws), workspace_bytes=ws.numel(),
         device_status=_ptr(st), stream=_stream(stream))
     raise_for(lib.pair_loss_sigmoid_fwd_bwd(ctypes.byref(args)), "pair_loss_sigmoid_fwd_bwd")
+    return dict(loss=loss, d_embeddings=de, d_inverse_temperature=dt, d_bias=db, device_status=st)
+
+
+def pair_loss_sigmoid_groups_fwd_bwd(embeddings, groups, inverse_temperature, bias, attract, repel=None, ignore=None,
+                                     negatives_named=False, ambient_weight=1.0, out=None, workspace=None,
+                                     device_status=None, stream=None):
+    """The pooled sigmoid pair loss with temperature groups: `groups` (int32 [N]) selects each item's pair of
+    `inverse_temperature`, `bias` (fp32 [G]) and a cell takes its anchor's.  Returns dict(loss, d_embeddings,
+    d_inverse_temperature [G], d_bias [G], device_status) of device tensors."""
+    _check_cuda(embeddings, "embeddings", torch.bfloat16)
+    _check_cuda(groups, "groups", torch.int32)
+    _check_cuda(inverse_temperature, "inverse_temperature", torch.float32)
+    _check_cuda(bias, "bias", torch.float32)
+    n, ld = embeddings.shape
+    g = inverse_temperature.numel()
+    if bias.numel() != g or groups.numel() != n:
+        raise ShapeMismatchError(CLI_SHAPE_MISMATCH, "groups, inverse_temperature and bias disagree in size")
+    width = (out or {}).get("width", ld)
+    dev = embeddings.device
+    out = dict(out or {})
+    loss = out.get("loss") if out.get("loss") is not None else torch.empty(1, device=dev)
+    de = out.get("d_embeddings") if out.get("d_embeddings") is not None else torch.empty(n, width, device=dev)
+    dt = out.get("d_inverse_temperature") if out.get("d_inverse_temperature") is not None else torch.empty(g, device=dev)
+    db = out.get("d_bias") if out.get("d_bias") is not None else torch.empty(g, device=dev)
+    st = device_status if device_status is not None else torch.zeros(1, dtype=torch.int32, device=dev)
+    A, R, I = _edges(attract, n), _edges(repel, n), _edges(ignore, n)
+    total = A.edges + R.edges + I.edges
+    need = pair_loss_sigmoid_workspace_bytes(n, width, total)
+    ws = workspace if workspace is not None else _ws(need, dev)
+    base = PairLossSigmoidArgs(
+        count=n, width=width, ld=embeddings.stride(0), embeddings=_ptr(embeddings),
+        inverse_temperature=_ptr(inverse_temperature), bias=_ptr(bias),
+        relations=Relations(A, R, I, int(bool(negatives_named)), float(ambient_weight)),
+        loss=_ptr(loss), d_embeddings=_ptr(de), ld_d_embeddings=de.stride(0),
+        d_inverse_temperature=_ptr(dt), d_bias=_ptr(db), workspace=_ptr(ws), workspace_bytes=ws.numel(),
+        device_status=_ptr(st), stream=_stream(stream))
+    args = PairLossGroupsArgs(base=base, groups=_ptr(groups), group_count=g)
+    raise_for(lib.pair_loss_sigmoid_groups_fwd_bwd(ctypes.byref(args)), "pair_loss_sigmoid_groups_fwd_bwd")
     return dict(loss=loss, d_embeddings=de, d_inverse_temperature=dt, d_bias=db, device_status=st)
 
 

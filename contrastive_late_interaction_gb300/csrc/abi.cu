@@ -123,14 +123,18 @@ cli_status_t pooled_checks(const cli_pair_loss_sigmoid_t *a, size_t &edges) {
 }
 
 // True when an output of a pooled call (the workspace taken as ws_bytes, plus
-// an optional extra output range) overlaps an input or another output.
-bool pooled_overlap(const cli_pair_loss_sigmoid_t *a, size_t ws_bytes, Range extra) {
+// an optional extra output range) overlaps an input or another output; `pairs`
+// is the number of (t, b) pairs (and of their gradients), `extra_in` an
+// optional extra input range.
+bool pooled_overlap(const cli_pair_loss_sigmoid_t *a, size_t ws_bytes, Range extra, size_t pairs = 1,
+                    Range extra_in = Range{0, 0}) {
     const cli_relations_t &rel = a->relations;
     const size_t n = a->count;
     const Range inputs[] = {
         range_of(a->embeddings, ((n - 1) * a->ld + a->width) * 2),
-        range_of(a->inverse_temperature, 4),
-        range_of(a->bias, 4),
+        range_of(a->inverse_temperature, 4 * pairs),
+        range_of(a->bias, 4 * pairs),
+        extra_in,
         range_of(rel.attract.offsets, edge_bytes(rel.attract, n)),
         range_of(rel.attract.ids, rel.attract.offsets ? rel.attract.edges * 4 : 0),
         range_of(rel.attract.weights, rel.attract.offsets && rel.attract.weights ? rel.attract.edges * 4 : 0),
@@ -143,8 +147,8 @@ bool pooled_overlap(const cli_pair_loss_sigmoid_t *a, size_t ws_bytes, Range ext
     const Range outputs[] = {
         range_of(a->loss, 4),
         range_of(a->d_embeddings, ((n - 1) * a->ld_d_embeddings + a->width) * 4),
-        range_of(a->d_inverse_temperature, 4),
-        range_of(a->d_bias, 4),
+        range_of(a->d_inverse_temperature, 4 * pairs),
+        range_of(a->d_bias, 4 * pairs),
         range_of(a->workspace, ws_bytes),
         range_of(a->device_status, 4),
         extra,
@@ -209,6 +213,53 @@ cli_status_t pair_loss_sigmoid_fwd_bwd(const cli_pair_loss_sigmoid_t *a) {
     const PooledLaunch L = pooled_launch_record(a, ws, static_cast<int>(a->width), a->d_embeddings,
                                                 static_cast<long long>(a->ld_d_embeddings), a->loss,
                                                 a->d_inverse_temperature, a->d_bias, sms);
+    if (launch_pooled_fused(tmap, L, stream) != cudaSuccess) return CLI_DEVICE;
+    return CLI_OK;
+}
+
+// ----------------------------------------------------------------------------
+// temperature groups of the pooled sigmoid pair loss
+// ----------------------------------------------------------------------------
+
+cli_status_t pair_loss_sigmoid_groups_fwd_bwd(const cli_pair_loss_groups_t *g) {
+    if (!g) return CLI_INVALID_ARGUMENT;
+    const cli_pair_loss_sigmoid_t *a = &g->base;
+    const cli_relations_t &rel = a->relations;
+    size_t edges = 0;
+    const cli_status_t st = pooled_checks(a, edges);
+    if (st != CLI_OK) return st;
+    if (!g->groups || !aligned(g->groups, 4)) return CLI_INVALID_ARGUMENT;
+    if (g->group_count == 0 || g->group_count >= (1ull << 31)) return CLI_SHAPE_MISMATCH;
+    const PooledWorkspace ws = carve_pooled_workspace(a->workspace, a->count, a->width, edges);
+    if (a->workspace_bytes < ws.bytes) return CLI_INVALID_ARGUMENT;
+    if (pooled_overlap(a, ws.bytes, Range{0, 0}, g->group_count, range_of(g->groups, a->count * 4)))
+        return CLI_INVALID_ARGUMENT;
+
+    const int sms = sm_count();
+    if (sms <= 0) return CLI_DEVICE;
+    const size_t n = a->count;
+    cudaStream_t stream = static_cast<cudaStream_t>(a->stream);
+    CUtensorMap tmap;
+    if (!encode_bf16_rows(&tmap, a->embeddings, a->width, n, a->ld)) return CLI_DEVICE;
+    if (cudaMemsetAsync(a->device_status, 0, sizeof(int32_t), stream) != cudaSuccess) return CLI_DEVICE;
+    if (launch_validate_groups(g->groups, static_cast<int>(n), static_cast<int>(g->group_count), a->device_status,
+                               stream) != cudaSuccess)
+        return CLI_DEVICE;
+    const EdgeSet sets[3] = {to_set(rel.attract), to_set(rel.repel), to_set(rel.ignore)};
+    if (launch_relation_prep(sets, static_cast<int>(n), rel.negatives_named, rel.ambient_weight, ws, a->device_status,
+                             stream) != cudaSuccess)
+        return CLI_DEVICE;
+    if (cudaMemset2DAsync(a->d_embeddings, a->ld_d_embeddings * 4, 0, a->width * 4, n, stream) != cudaSuccess)
+        return CLI_DEVICE;
+    PooledLaunch L = pooled_launch_record(a, ws, static_cast<int>(a->width), a->d_embeddings,
+                                          static_cast<long long>(a->ld_d_embeddings), a->loss,
+                                          a->d_inverse_temperature, a->d_bias, sms);
+    if (g->group_count > 1) {   // one group is the symmetric call
+        if (cudaMemsetAsync(a->d_inverse_temperature, 0, g->group_count * 4, stream) != cudaSuccess ||
+            cudaMemsetAsync(a->d_bias, 0, g->group_count * 4, stream) != cudaSuccess)
+            return CLI_DEVICE;
+        L.group = g->groups;
+    }
     if (launch_pooled_fused(tmap, L, stream) != cudaSuccess) return CLI_DEVICE;
     return CLI_OK;
 }

@@ -59,6 +59,10 @@ struct PooledLaunch {
     float *loss, *dt, *db;
     int32_t *status;
     int sm_count;
+    // Temperature groups: item i's group (device, validated), or null for one
+    // (t, b).  With groups, t_ptr and b_ptr index by group and dt, db are
+    // per-group arrays that the kernel adds into (zeroed by the caller).
+    const int32_t *group = nullptr;
 };
 
 // Relation preparation: validation, transposition and merged special lists.
@@ -151,6 +155,7 @@ bool encode_bf16_tiles(CUtensorMap *map, const void *base, uint64_t cols, uint64
 
 // Shared validation kernels.
 cudaError_t launch_validate_edges(const EdgeSet &set, int n, int id_limit, int32_t *status, cudaStream_t stream);
+cudaError_t launch_validate_groups(const int32_t *group, int n, int groups, int32_t *status, cudaStream_t stream);
 cudaError_t launch_validate_tape(const uint64_t *offsets, int count, uint64_t rows, int32_t *status,
                                  cudaStream_t stream);
 

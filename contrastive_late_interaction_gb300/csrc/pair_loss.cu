@@ -87,6 +87,10 @@ struct Params {
     long long ld_de;
     float *partials;   // [blocks][kEpiWarps][4]
     int32_t *status;
+    // Temperature groups (null when one pair serves every cell): item i's group,
+    // the per-group gradients (accumulated), and the mode's full grid of blocks.
+    const int32_t *group;
+    float *dt_g, *db_g;
 };
 
 // Pair p -> (I, J), I <= J, over an n x n grid.  The upper triangle is walked
@@ -155,11 +159,16 @@ struct Block {
 
 __device__ __forceinline__ Block decode_block(long long p, const Params &P) {
     int bi, bj;
-    decode_pair(p, P.nbb, bi, bj);
+    if (P.group) {   // every ordered block, each cell scored for its row's anchor only
+        bi = static_cast<int>(p / P.nbb);
+        bj = static_cast<int>(p % P.nbb);
+    } else {
+        decode_pair(p, P.nbb, bi, bj);
+    }
     Block b;
     b.I0 = 2 * bi;
     b.J0 = 2 * bj;
-    b.diag = bi == bj;
+    b.diag = bi == bj && !P.group;
     b.i1 = b.I0 + 1 < P.nb;
     b.j1 = b.J0 + 1 < P.nb;
     return b;
@@ -486,11 +495,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int x = ew >> 2;                   // tile row of the block this warp reads (and drains)
         const int row = quad * 32 + lane;        // row of the tile this thread owns
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const float t = *P.t_ptr, b = *P.b_ptr;
-        const float t2 = t * kLog2e, b2 = b * kLog2e;
         const float inv_n = 1.0f / static_cast<float>(P.n);
-        const float c_h = t * inv_n;             // H = (t/N) G
         const float w_d = P.named ? 0.0f : P.ambient;
+        // A visited cell serves both ordered pairs, or (with groups) its row's anchor only.
+        const float dirs = P.group ? 1.0f : 2.0f;
+        const float w_dd = dirs * w_d;
         const uint32_t stage_s = smem_u32(sm.stage_t[ew]);
         uint32_t kblk = 0, chunk = 0;
         for (long long p = blockIdx.x; p < P.blocks; p += gridDim.x, ++kblk) {
@@ -499,6 +508,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int gi = (bk.I0 + x) * BM + row;   // this thread's item (anchor)
             const bool row_ok = x_on && gi < P.n;
             const int y_first = (bk.diag && x == 1) ? 1 : 0;
+            // This row's (t, b): the run's pair, or its anchor's group's.
+            const int grp = (P.group && row_ok) ? P.group[gi] : 0;
+            const float t = P.t_ptr[grp], b = P.b_ptr[grp];
+            const float t2 = t * kLog2e, b2 = b * kLog2e;
+            const float c_h = t * inv_n;             // H = (t/N) G
             // This row's special columns from the first tile column it reads on.
             uint32_t e = 0, e_end = 0;
             if (row_ok) {
@@ -520,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int slot = 2 * x + y;
                 const int j0 = (bk.J0 + y) * BM;
                 const uint32_t hbase = smem_u32(sm.hreg[2 * slot]);
-                float acc_sp = 0.f, acc_p = 0.f, acc_ps = 0.f;   // default cells (times 2 w_d later)
+                float acc_sp = 0.f, acc_p = 0.f, acc_ps = 0.f;   // default cells (times dirs w_d later)
                 float fix_l = 0.f, fix_g = 0.f, fix_gs = 0.f;   // corrections for special cells
 #pragma unroll 1
                 for (int ch = 0; ch < BM / 32; ++ch) {
@@ -538,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float za = fmaf(t, smin, b), zb = fmaf(t, smax, b);
                     const float zlo = fminf(za, zb), zhi = fmaxf(za, zb);
                     float hv[32];
-                    const float hscale = c_h * 2.0f * w_d;
+                    const float hscale = c_h * w_dd;
                     const bool full = __all_sync(0xffffffffu, row_ok && valid == 32);
                     const bool negfar = __all_sync(0xffffffffu, zhi <= -kFarZ);
                     const bool far = __all_sync(0xffffffffu, zhi <= -kFarZ || zlo >= kFarZ);
@@ -564,10 +578,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float z = fmaf(t, s, b);
                         const CellFn f = cell_fn(z);
                         const bool ao = en.flags & 1u, ai = en.flags & 2u;
-                        const float g = en.w_out * (ao ? -f.pc : f.p) + en.w_in * (ai ? -f.pc : f.p);
-                        const float l = en.w_out * (ao ? f.sp - z : f.sp) + en.w_in * (ai ? f.sp - z : f.sp);
-                        const float g_def = 2.0f * w_d * f.p;
-                        fix_l += l - 2.0f * w_d * f.sp;
+                        const float w_in = P.group ? 0.0f : en.w_in;   // (j, i) is its own visit with groups
+                        const float g = en.w_out * (ao ? -f.pc : f.p) + w_in * (ai ? -f.pc : f.p);
+                        const float l = en.w_out * (ao ? f.sp - z : f.sp) + w_in * (ai ? f.sp - z : f.sp);
+                        const float g_def = w_dd * f.p;
+                        fix_l += l - w_dd * f.sp;
                         fix_g += g - g_def;
                         fix_gs += (g - g_def) * s;
                         const float hnew = c_h * g;
@@ -585,9 +600,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // A diagonal tile sees every unordered pair twice.
                 const float scale = (bk.diag && x == y) ? 0.5f : 1.0f;
-                l_sum += scale * (2.0f * w_d * acc_sp + fix_l);
-                g_sum += scale * (2.0f * w_d * acc_p + fix_g);
-                gs_sum += scale * (2.0f * w_d * acc_ps + fix_gs);
+                l_sum += scale * (w_dd * acc_sp + fix_l);
+                g_sum += scale * (w_dd * acc_p + fix_g);
+                gs_sum += scale * (w_dd * acc_ps + fix_gs);
+            }
+            if (P.group) {   // this row's cells belong to its group's (t, b)
+                if (row_ok && (g_sum != 0.f || gs_sum != 0.f)) {
+                    atomicAdd(P.dt_g + grp, gs_sum * inv_n);
+                    atomicAdd(P.db_g + grp, g_sum * inv_n);
+                }
+                g_sum = gs_sum = 0.f;
             }
             tc_fence_before();
             fence_proxy_async_smem();
@@ -699,21 +721,22 @@ __global__ void finish_kernel(const double *sums, int n, float *loss, float *dt,
     if (threadIdx.x == 0) {
         const double inv_n = 1.0 / static_cast<double>(n);
         *loss = static_cast<float>(red[0][0] * inv_n);
-        *dt = static_cast<float>(red[1][0] * inv_n);
-        *db = static_cast<float>(red[2][0] * inv_n);
+        if (dt) *dt = static_cast<float>(red[1][0] * inv_n);   // with groups the kernel sums them per group
+        if (db) *db = static_cast<float>(red[2][0] * inv_n);
     }
 }
 
-long long block_count(int n) {
+// Blocks of one call: the upper triangle, or every ordered block with groups.
+long long block_count(int n, bool groups) {
     const long long nb = (n + BM - 1) / BM, nbb = (nb + 1) / 2;
-    return nbb * (nbb + 1) / 2;
+    return groups ? nbb * nbb : nbb * (nbb + 1) / 2;
 }
 
 }  // namespace pooled
 
 size_t pooled_fused_smem_bytes() { return pooled::kSmemBytes; }
 
-long long pooled_partial_slots(int n) { return pooled::block_count(n) * pooled::kPartialsPerBlock; }
+long long pooled_partial_slots(int n) { return pooled::block_count(n, true) * pooled::kPartialsPerBlock; }
 int pooled_finish_blocks() { return pooled::kFinishBlocks; }
 
 cudaError_t launch_pooled_fused(const CUtensorMap &tmap_e, const PooledLaunch &L, cudaStream_t stream) {
@@ -731,7 +754,10 @@ cudaError_t launch_pooled_fused(const CUtensorMap &tmap_e, const PooledLaunch &L
     P.nk = (L.width + BK - 1) / BK;
     P.nb = (L.n + BM - 1) / BM;
     P.nbb = (P.nb + 1) / 2;
-    P.blocks = block_count(L.n);
+    P.blocks = block_count(L.n, L.group != nullptr);
+    P.group = L.group;
+    P.dt_g = L.group ? L.dt : nullptr;
+    P.db_g = L.group ? L.db : nullptr;
     P.t_ptr = L.t_ptr;
     P.b_ptr = L.b_ptr;
     P.ambient = L.ambient;
@@ -749,7 +775,8 @@ cudaError_t launch_pooled_fused(const CUtensorMap &tmap_e, const PooledLaunch &L
     if (err != cudaSuccess) return err;
     finish_partial_kernel<<<kFinishBlocks, 256, 0, stream>>>(L.partials, P.blocks * kPartialsPerBlock, L.sums, L.status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    finish_kernel<<<1, kFinishBlocks, 0, stream>>>(L.sums, L.n, L.loss, L.dt, L.db, L.status);
+    finish_kernel<<<1, kFinishBlocks, 0, stream>>>(L.sums, L.n, L.loss, L.group ? nullptr : L.dt,
+                                                   L.group ? nullptr : L.db, L.status);
     return cudaGetLastError();
 }
 

@@ -64,6 +64,12 @@ __global__ void validate_tape_kernel(const uint64_t *off, int count, uint64_t ro
     else if (a == b) report(status, CLI_INVALID_ARGUMENT);  // an empty query or document has no max
 }
 
+// Every item's temperature group lies in [0, groups).
+__global__ void validate_groups_kernel(const int32_t *group, int n, int groups, int32_t *status) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n && (group[i] < 0 || group[i] >= groups)) report(status, CLI_MALFORMED);
+}
+
 __global__ void count_indegree_kernel(EdgeSet a, EdgeSet r, EdgeSet g, int n, uint32_t *indeg, const int32_t *status) {
     if (read_status(status) != 0) return;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -289,6 +295,11 @@ cudaError_t launch_validate_edges(const EdgeSet &set, int n, int id_limit, int32
 cudaError_t launch_validate_tape(const uint64_t *offsets, int count, uint64_t rows, int32_t *status,
                                  cudaStream_t stream) {
     validate_tape_kernel<<<blocks_for(count, 256), 256, 0, stream>>>(offsets, count, rows, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_validate_groups(const int32_t *group, int n, int groups, int32_t *status, cudaStream_t stream) {
+    validate_groups_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(group, n, groups, status);
     return cudaGetLastError();
 }
 

@@ -48,6 +48,7 @@ STREAM_D_SCORES = 8
 STREAM_SIDES = 9
 STREAM_WEIGHTS = 10
 STREAM_ARGMAX = 11
+STREAM_GROUPS = 12
 
 
 def _mix(z: np.ndarray) -> np.ndarray:

@@ -144,6 +144,36 @@ cli_status_t pair_loss_sigmoid_fwd_bwd(const cli_pair_loss_sigmoid_t *args);
 size_t pair_loss_sigmoid_workspace_bytes(size_t count, size_t width, size_t edges);
 
 /*
+ * pair_loss_sigmoid_groups_fwd_bwd -- the pooled sigmoid pair loss with
+ * temperature groups ("Training", `uform_contrastive_t`, `temperature_groups`:
+ * learnable (inverse temperature, bias) pairs, one per group a step's items
+ * select).  Item i selects group g(i), and a cell takes its anchor's pair:
+ *     z_ij = t[g(i)] <e_i, e_j> + b[g(i)],  l_ij = w_ij softplus(-y_ij z_ij),
+ *     L = (1/N) sum_{i != j} l_ij,  dE, and dt[g], db[g] per group.
+ *
+ *   base            every field as in cli_pair_loss_sigmoid_t, except that
+ *                   inverse_temperature, bias are device fp32 [group_count]
+ *                   and d_inverse_temperature, d_bias device fp32
+ *                   [group_count] (written); the workspace is sized by
+ *                   pair_loss_sigmoid_workspace_bytes
+ *   groups          device int32 [count], item i's group; a value outside
+ *                   [0, group_count) sets CLI_MALFORMED in the device status
+ *   group_count     at least 1
+ *
+ * With one group the call is pair_loss_sigmoid_fwd_bwd.  With more, z is not
+ * symmetric, so every ordered pair of tiles is visited (twice the tensor work)
+ * and the per-group dt, db are summed with atomic adds: they reproduce to
+ * rounding, not bit for bit.
+ */
+typedef struct {
+    cli_pair_loss_sigmoid_t base;
+    const int32_t *groups;
+    size_t group_count;
+} cli_pair_loss_groups_t;
+
+cli_status_t pair_loss_sigmoid_groups_fwd_bwd(const cli_pair_loss_groups_t *args);
+
+/*
  * pair_loss_sigmoid_matryoshka_fwd_bwd -- the pooled sigmoid pair loss over
  * nested prefixes of the embeddings ("Training", `uform_contrastive_t`,
  * `matryoshka_dimensions`: prefix widths strictly ascending, each a multiple

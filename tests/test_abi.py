@@ -188,3 +188,19 @@ def test_matryoshka_host_checks(b):
     assert f([64], workspace_bytes=b.pair_loss_sigmoid_workspace_bytes(n, w, 2048)) == b.CLI_INVALID_ARGUMENT
     assert f([64], prefix_loss=A * 1) == b.CLI_INVALID_ARGUMENT          # an output inside the embeddings
     assert f([64], embeddings=None) == b.CLI_INVALID_ARGUMENT            # the pooled checks still apply
+
+
+def test_groups_host_checks(b):
+    n, w = 1024, 512
+
+    def f(groups=A * 13, count=3, **over):
+        args = b.PairLossGroupsArgs(base=pooled_args(b, **over), groups=groups, group_count=count)
+        return b.lib.pair_loss_sigmoid_groups_fwd_bwd(ctypes.byref(args))
+
+    assert b.lib.pair_loss_sigmoid_groups_fwd_bwd(None) == b.CLI_INVALID_ARGUMENT
+    assert f(groups=None) == b.CLI_INVALID_ARGUMENT
+    assert f(groups=A * 13 + 2) == b.CLI_INVALID_ARGUMENT                # not 4-byte aligned
+    assert f(count=0) == b.CLI_SHAPE_MISMATCH
+    assert f(groups=A * 7) == b.CLI_INVALID_ARGUMENT                     # an input inside the dE output
+    assert f(count=3, d_bias=A * 8 + 8) == b.CLI_INVALID_ARGUMENT        # d_bias [3] overlaps d_inverse_temperature [3]
+    assert f(count=3, embeddings=None) == b.CLI_INVALID_ARGUMENT         # the pooled checks still apply
