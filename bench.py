@@ -42,7 +42,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["joint", "pooled2", "maxsim3", "pooled4", "matryoshka5", "groups5"], default="joint")
+    ap.add_argument("--workload", choices=["joint", "pooled2", "maxsim3", "pooled4", "matryoshka5", "groups5", "named5"], default="joint")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work budget of the oracle baseline")
@@ -67,6 +67,11 @@ def make_workload(name: str, seed: int):
     if name == "matryoshka5":
         # the joint step's pooled batch scored at the nested prefixes {64, 128, 256, 512}
         return dict(pooled=synth.joint_config5(seed).pooled, maxsim=None, joint=None, prefixes=[64, 128, 256, 512])
+    if name == "named5":
+        # the joint step's MaxSim tapes, each query naming its own document and seven others
+        j = synth.joint_config5(seed)
+        att, rep = synth.named_documents(seed, j.maxsim.nq, j.maxsim.nd, 7)
+        return dict(pooled=None, maxsim=j.maxsim, joint=None, prefixes=None, named=(att, rep))
     if name == "groups5":
         # the joint step's pooled batch with four temperature groups drawn uniformly per item
         p = synth.joint_config5(seed).pooled
@@ -81,12 +86,28 @@ def pooled_flops(p, prefixes=None):
     return sum(3.0 * p.count * p.count * w for w in (prefixes or [p.width]))
 
 
-def maxsim_fwd_flops(m):
-    return 2.0 * m.width * float(m.q_offsets[-1]) * float(m.d_offsets[-1])
+def _named_pairs(m, named):
+    """(query, document) index arrays of the named pairs."""
+    q = np.concatenate([np.repeat(np.arange(m.nq), np.diff(e.offsets).astype(np.int64)) for e in named])
+    d = np.concatenate([e.ids.astype(np.int64) for e in named])
+    return q, d
 
 
-def maxsim_bwd_flops(m):
-    return 4.0 * m.width * float(m.q_offsets[-1]) * m.nd
+def maxsim_fwd_flops(m, named=None):
+    """2 D |q| |d| per scored (query, document) pair: every pair, or the named ones."""
+    if named is None:
+        return 2.0 * m.width * float(m.q_offsets[-1]) * float(m.d_offsets[-1])
+    q, d = _named_pairs(m, named)
+    return float(np.sum(2.0 * m.width * np.diff(m.q_offsets)[q].astype(np.float64) *
+                        np.diff(m.d_offsets)[d].astype(np.float64)))
+
+
+def maxsim_bwd_flops(m, named=None):
+    """4 D |q| per scored pair (one gathered row each for dQ and dD, times c)."""
+    if named is None:
+        return 4.0 * m.width * float(m.q_offsets[-1]) * m.nd
+    q, _ = _named_pairs(m, named)
+    return float(np.sum(4.0 * m.width * np.diff(m.q_offsets)[q].astype(np.float64)))
 
 
 def describe(name, w):
@@ -94,7 +115,8 @@ def describe(name, w):
                         "pooled4": "large pooled sigmoid loss (config 4)",
                         "maxsim3": "MaxSim fwd+bwd (config 3)",
                         "matryoshka5": "Matryoshka prefixes of the pooled sigmoid loss (config 5 pooled batch)",
-                        "groups5": "pooled sigmoid loss with four temperature groups (config 5 pooled batch)"}[name]}
+                        "groups5": "pooled sigmoid loss with four temperature groups (config 5 pooled batch)",
+                        "named5": "MaxSim fwd+bwd over named pairs (config 5 tapes, own document + 7 named)"}[name]}
     p, m = w["pooled"], w["maxsim"]
     if p is not None:
         cfg["pooled"] = {"N": p.count, "D": p.width, "t": p.t, "b": p.b,
@@ -108,6 +130,10 @@ def describe(name, w):
     if m is not None:
         cfg["maxsim"] = {"queries": m.nq, "documents": m.nd, "D": m.width, "query_rows": int(m.q_offsets[-1]),
                          "document_rows": int(m.d_offsets[-1]), "form": "mean" if m.mean else "sum"}
+        if w.get("named"):
+            cfg["maxsim"]["named_pairs"] = int(w["named"][0].ids.size + w["named"][1].ids.size)
+            cfg["score_loss"] = {"t": 1.0, "b": 0.0, "attract": "own document", "repel": "7 named documents",
+                                 "negatives": "named"}
     if w["joint"] is not None:
         cfg["score_loss"] = {"t": w["joint"].score_t, "b": w["joint"].score_b, "attract": "(i, i)",
                              "sides": "query/document/both, 1/3 each"}
@@ -129,6 +155,7 @@ class Step:
         self.p, self.m, self.j = w["pooled"], w["maxsim"], w["joint"]
         self.prefixes = w.get("prefixes")
         self.groups = w.get("groups")
+        self.named = w.get("named")
         self.host = {}      # pinned host copies for the end-to-end measurement
         self.dev_in = {}
         with torch.cuda.stream(stream):
@@ -201,6 +228,24 @@ class Step:
                 self.s_out = dict(loss=torch.empty(1, **f32), d_scores=torch.empty(m.nq, m.nd, **f32),
                                   d_inverse_temperature=torch.empty(1, **f32), d_bias=torch.empty(1, **f32))
                 self.s_st = torch.zeros(1, dtype=torch.int32, device=self.dev)
+            elif self.named:
+                att, rep = self.named
+                lists = [sorted(att.ids[att.offsets[q]:att.offsets[q + 1]].tolist() +
+                                rep.ids[rep.offsets[q]:rep.offsets[q + 1]].tolist()) for q in range(m.nq)]
+                from contrastive_late_interaction_gb300 import synth
+                pairs = synth.edges_from_lists(lists)
+                self.pairs = (self._pin("pair_off", pairs.offsets), self._pin("pair_ids", pairs.ids))
+                self.n_att = (self._pin("natt_off", att.offsets), self._pin("natt_ids", att.ids))
+                self.n_rep = (self._pin("nrep_off", rep.offsets), self._pin("nrep_ids", rep.ids))
+                self.st_ = self._pin("st", np.array([1.0], np.float32))
+                self.sb_ = self._pin("sb", np.array([0.0], np.float32))
+                self.f_ws = torch.empty(cli.maxsim_named_workspace_bytes(m.nq, m.nd, rq, rd, m.width),
+                                        dtype=torch.uint8, device=self.dev)
+                self.s_ws = torch.empty(cli.pair_loss_sigmoid_scores_workspace_bytes(m.nq, m.nd), dtype=torch.uint8,
+                                        device=self.dev)
+                self.s_out = dict(loss=torch.empty(1, **f32), d_scores=torch.empty(m.nq, m.nd, **f32),
+                                  d_inverse_temperature=torch.empty(1, **f32), d_bias=torch.empty(1, **f32))
+                self.s_st = torch.zeros(1, dtype=torch.int32, device=self.dev)
             else:
                 self.ds = self._pin("ds", m.d_scores)
 
@@ -219,6 +264,9 @@ class Step:
         if self.m is not None:
             n += 2 + 1 + 1 + 1                            # 2 tape validations, schedule, forward, query sums
             n += 2 + 1 + 1 + 1                            # 2 tape validations, row->query map, dQ, dD
+            if self.named:
+                n += 1 + 1 + 1 + 1                        # pair validation, item marks, compaction, score mask
+                n += 2 + 1 + 1                            # 2 edge validations, score loss, final reduction
             if self.j is not None:
                 n += 1 + 1 + 1                            # edge validation, score loss, final reduction
         return n
@@ -248,10 +296,21 @@ class Step:
                 rec("pooled", 1)
             if self.m is not None:
                 rec("maxsim_fwd", 0)
-                f = cli.maxsim_scores(self.q, self.qo, self.d, self.do, out=self.f_out, workspace=self.f_ws,
-                                      device_status=self.f_st, stream=self.stream)
+                if self.named:
+                    f = cli.maxsim_scores_named(self.q, self.qo, self.d, self.do, self.pairs, out=self.f_out,
+                                                workspace=self.f_ws, device_status=self.f_st, stream=self.stream)
+                else:
+                    f = cli.maxsim_scores(self.q, self.qo, self.d, self.do, out=self.f_out, workspace=self.f_ws,
+                                          device_status=self.f_st, stream=self.stream)
                 rec("maxsim_fwd", 1)
-                if self.j is not None:
+                if self.named:
+                    rec("score_loss", 0)
+                    s = cli.pair_loss_sigmoid_scores_fwd_bwd(f["scores"], self.st_, self.sb_, self.n_att, self.n_rep,
+                                                             negatives_named=True, out=self.s_out, workspace=self.s_ws,
+                                                             device_status=self.s_st, stream=self.stream)
+                    rec("score_loss", 1)
+                    ds = s["d_scores"]
+                elif self.j is not None:
                     rec("score_loss", 0)
                     s = cli.pair_loss_sigmoid_scores_fwd_bwd(f["scores"], self.st_, self.sb_, self.diag,
                                                              sides=self.sides, out=self.s_out, workspace=self.s_ws,
@@ -276,7 +335,7 @@ class Step:
         outs = []
         if self.p is not None:
             outs += [self.p_out["loss"], self.p_out["d_inverse_temperature"], self.p_out["d_bias"]]
-        if self.j is not None:
+        if self.j is not None or self.named:
             outs += [self.s_out["loss"], self.s_out["d_inverse_temperature"], self.s_out["d_bias"]]
         return outs
 
@@ -428,7 +487,12 @@ def oracle_sample(w, budget_s: float, threads: int):
         k = 16
         q, d = m.q, m.d
         while True:
-            pq, pd = rng.integers(0, m.nq, k), rng.integers(0, m.nd, k)
+            if w.get("named"):   # a sample of the named pairs
+                nq_all, nd_all = _named_pairs(m, w["named"])
+                pick = rng.integers(0, nq_all.size, k)
+                pq, pd = nq_all[pick], nd_all[pick]
+            else:
+                pq, pd = rng.integers(0, m.nq, k), rng.integers(0, m.nd, k)
             t0 = time.perf_counter()
             oracle.maxsim_pairs(m.q_offsets, q, m.d_offsets, d, pq, pd, threads=threads)
             dt = time.perf_counter() - t0
@@ -439,7 +503,8 @@ def oracle_sample(w, budget_s: float, threads: int):
         dl = (m.d_offsets[pd + 1] - m.d_offsets[pd]).astype(np.float64)
         flops += float(np.sum(2.0 * m.width * ql * dl + 4.0 * m.width * ql))
         secs += dt
-        desc.append(f"MaxSim: {k} random (query, document) pairs of {m.nq}x{m.nd}")
+        desc.append(f"MaxSim: {k} random (query, document) pairs of {m.nq}x{m.nd}" +
+                    (" among the named ones" if w.get("named") else ""))
     return flops, secs, "; ".join(desc)
 
 
@@ -519,7 +584,8 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     names = [n for n in ("pooled", "maxsim_fwd", "score_loss", "maxsim_bwd")
              if (n == "pooled" and step.p is not None) or (n != "pooled" and step.m is not None and
-                                                          (n != "score_loss" or step.j is not None))]
+                                                          (n != "score_loss" or step.j is not None or
+                                                           step.named is not None))]
 
     for _ in range(max(3, args.warmup)):
         step.run()
@@ -552,7 +618,7 @@ def main():
     p, m = step.p, step.m
     pre = w.get("prefixes")
     flops = (pooled_flops(p, pre) if p is not None else 0.0) + \
-            ((maxsim_fwd_flops(m) + maxsim_bwd_flops(m)) if m is not None else 0.0)
+            ((maxsim_fwd_flops(m, w.get("named")) + maxsim_bwd_flops(m, w.get("named"))) if m is not None else 0.0)
     ms, value = aggregate(pg, world, flops, statistics.mean(step_ms), device)
     burst, sustained, hbm, peak_src = peaks()
     parts = {}
@@ -563,23 +629,23 @@ def main():
                               "frac_of_peak": pooled_flops(p, pre) / (pm * 1e-3) / 1e12 / sustained}
     if m is not None:
         fm, bm = statistics.mean(part_ms["maxsim_fwd"]), statistics.mean(part_ms["maxsim_bwd"])
-        tf = (maxsim_fwd_flops(m) + maxsim_bwd_flops(m)) / ((fm + bm) * 1e-3) / 1e12
+        tf = (maxsim_fwd_flops(m, w.get("named")) + maxsim_bwd_flops(m, w.get("named"))) / ((fm + bm) * 1e-3) / 1e12
         parts["maxsim"] = {"fwd_ms": fm, "bwd_ms": bm, "tflops_fwd_bwd": tf, "frac_of_peak": tf / sustained,
-                           "fwd_tflops": maxsim_fwd_flops(m) / (fm * 1e-3) / 1e12,
+                           "fwd_tflops": maxsim_fwd_flops(m, w.get("named")) / (fm * 1e-3) / 1e12,
                            "bwd_gathered_gb_per_s": 2 * 2.0 * m.width * float(m.q_offsets[-1]) * m.nd / (bm * 1e-3) / 1e9}
-        if step.j is not None:
+        if step.j is not None or step.named is not None:
             parts["score_loss"] = {"ms": statistics.mean(part_ms["score_loss"])}
 
     # roofline: the dominant kernel (by time) of the step
     if m is not None:
         fm = statistics.mean(part_ms["maxsim_fwd"])
-        achieved = maxsim_fwd_flops(m) / (fm * 1e-3) / 1e12
+        achieved = maxsim_fwd_flops(m, w.get("named")) / (fm * 1e-3) / 1e12
         roofline = {"kernel": "maxsim forward (maxsim_scores call: forward tile kernel + its schedule, tape "
                               "checks and query sums)",
                     "bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
                     "frac": achieved / sustained, "peak_source": f"{peak_src} bf16 sustained",
                     "traffic": committed_traffic(args.workload),
-                    "algorithmic_per_launch": maxsim_fwd_flops(m)}
+                    "algorithmic_per_launch": maxsim_fwd_flops(m, w.get("named"))}
     else:
         pm = statistics.mean(part_ms["pooled"])
         achieved = pooled_flops(p, pre) / (pm * 1e-3) / 1e12

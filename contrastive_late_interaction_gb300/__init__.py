@@ -13,7 +13,7 @@ _BINDING_NAMES = {
     "pair_loss_sigmoid_scores_workspace_bytes", "pair_loss_sigmoid_workspace_bytes", "status_name", "LIB_PATH",
     "raise_for", "pair_loss_scores_fwd_bwd", "pair_loss_scores_workspace_bytes",
     "pair_loss_sigmoid_matryoshka_fwd_bwd", "pair_loss_sigmoid_matryoshka_workspace_bytes",
-    "pair_loss_sigmoid_groups_fwd_bwd",
+    "pair_loss_sigmoid_groups_fwd_bwd", "maxsim_scores_named", "maxsim_named_workspace_bytes",
 }
 
 

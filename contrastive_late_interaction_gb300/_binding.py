@@ -123,6 +123,10 @@ class MaxSimArgs(ctypes.Structure):
                 ("stream", c_void_p)]
 
 
+class MaxSimNamedArgs(ctypes.Structure):
+    _fields_ = [("base", MaxSimArgs), ("pairs", Edges)]
+
+
 class MaxSimBackwardArgs(ctypes.Structure):
     _fields_ = [("queries", Tape), ("documents", Tape), ("width", c_size_t), ("mean", c_int),
                 ("argmax", c_void_p), ("ld_argmax", c_size_t), ("d_scores", c_void_p), ("ld_d_scores", c_size_t),
@@ -143,6 +147,8 @@ EXPORTS = {
     "pair_loss_scores_workspace_bytes": (c_size_t, [c_int, c_size_t, c_size_t]),
     "maxsim_scores": (c_int, [ctypes.POINTER(MaxSimArgs)]),
     "maxsim_workspace_bytes": (c_size_t, [c_size_t, c_size_t, c_size_t, c_size_t, c_size_t]),
+    "maxsim_scores_named": (c_int, [ctypes.POINTER(MaxSimNamedArgs)]),
+    "maxsim_named_workspace_bytes": (c_size_t, [c_size_t, c_size_t, c_size_t, c_size_t, c_size_t]),
     "maxsim_backward": (c_int, [ctypes.POINTER(MaxSimBackwardArgs)]),
     "maxsim_backward_workspace_bytes": (c_size_t, [c_size_t, c_size_t, c_size_t, c_size_t, c_size_t]),
     "maxsim_backward_no_alloc": (c_int, [ctypes.POINTER(MaxSimBackwardArgs)]),
@@ -446,6 +452,35 @@ def maxsim_scores(q_data, q_offsets, d_data, d_offsets, mean=False, out=None, wo
                       ld_scores=scores.stride(0), argmax=_ptr(argmax), ld_argmax=argmax.stride(0),
                       workspace=_ptr(ws), workspace_bytes=ws.numel(), device_status=_ptr(st), stream=_stream(stream))
     raise_for(lib.maxsim_scores(ctypes.byref(args)), "maxsim_scores")
+    return dict(scores=scores, argmax=argmax, device_status=st)
+
+
+def maxsim_named_workspace_bytes(nq, nd, rows_q, rows_d, width):
+    return int(lib.maxsim_named_workspace_bytes(nq, nd, rows_q, rows_d, width))
+
+
+def maxsim_scores_named(q_data, q_offsets, d_data, d_offsets, pairs, mean=False, out=None, workspace=None,
+                        device_status=None, stream=None):
+    """Hard MaxSim of each query against the documents `pairs` names (a CSR over the queries, as from
+    `device_edges`).  Returns dict(scores [nq, nd] fp32, zero for pairs not named, argmax [nd, rows_q] int32,
+    a valid row of the document for pairs not named, device_status)."""
+    Q, D = _tape(q_data, q_offsets), _tape(d_data, d_offsets)
+    width = q_data.shape[1]
+    if d_data.shape[1] != width:
+        raise ShapeMismatchError(CLI_SHAPE_MISMATCH, "maxsim_scores_named: query and document widths differ")
+    dev = q_data.device
+    out = dict(out or {})
+    scores = out.get("scores") if out.get("scores") is not None else torch.empty(Q.count, D.count, device=dev)
+    argmax = out.get("argmax") if out.get("argmax") is not None else torch.empty(D.count, Q.rows, dtype=torch.int32,
+                                                                                  device=dev)
+    st = device_status if device_status is not None else torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = workspace if workspace is not None else _ws(
+        maxsim_named_workspace_bytes(Q.count, D.count, Q.rows, D.rows, width), dev)
+    base = MaxSimArgs(queries=Q, documents=D, width=width, mean=int(bool(mean)), scores=_ptr(scores),
+                      ld_scores=scores.stride(0), argmax=_ptr(argmax), ld_argmax=argmax.stride(0),
+                      workspace=_ptr(ws), workspace_bytes=ws.numel(), device_status=_ptr(st), stream=_stream(stream))
+    args = MaxSimNamedArgs(base=base, pairs=_edges(pairs, Q.count))
+    raise_for(lib.maxsim_scores_named(ctypes.byref(args)), "maxsim_scores_named")
     return dict(scores=scores, argmax=argmax, device_status=st)
 
 

@@ -495,13 +495,17 @@ struct MaxSimWs {
     int n_chunks, chunk_rows;
 };
 
-MaxSimWs carve_maxsim(void *base, size_t nd, size_t rows_q, size_t rows_d, int sms) {
+// Named pairs run on the finest chunks (1024 document rows), so that items
+// holding no named pair are skipped at a fine grain.
+constexpr int kNamedChunkRows = 1024;
+
+MaxSimWs carve_maxsim(void *base, size_t nd, size_t rows_q, size_t rows_d, int sms, bool named = false) {
     MaxSimWs w;
     uint8_t *p = static_cast<uint8_t *>(base);
     size_t off = 0;
     w.mval = reinterpret_cast<float *>(p ? p + off : nullptr);
     off += align256(nd * rows_q * sizeof(float));
-    w.chunk_rows = chunk_rows_for(rows_d, rows_q, sms > 0 ? sms : 148);
+    w.chunk_rows = named ? kNamedChunkRows : chunk_rows_for(rows_d, rows_q, sms > 0 ? sms : 148);
     w.n_chunks = static_cast<int>((rows_d + w.chunk_rows - 1) / w.chunk_rows);
     w.chunk_doc = reinterpret_cast<uint32_t *>(p ? p + off : nullptr);
     off += align256((static_cast<size_t>(w.n_chunks) + 1) * sizeof(uint32_t));
@@ -520,7 +524,19 @@ size_t maxsim_workspace_bytes(size_t query_count, size_t document_count, size_t 
     return align256(document_count * query_rows * sizeof(float)) + align256((chunks + 1) * sizeof(uint32_t));
 }
 
-cli_status_t maxsim_scores(const cli_maxsim_t *a) {
+}  // extern "C"
+
+namespace cli {
+namespace {
+
+// Work items of the named-pair schedule at most: chunks of kNamedChunkRows rows
+// times 128-row query blocks.
+size_t named_items_max(size_t query_rows, size_t document_rows) {
+    return ((document_rows + kNamedChunkRows - 1) / kNamedChunkRows + 1) * ((query_rows + 127) / 128);
+}
+
+// maxsim_scores, over every pair (pairs null) or the named ones.
+cli_status_t maxsim_forward_call(const cli_maxsim_t *a, const cli_edges_t *pairs) {
     if (!a) return CLI_INVALID_ARGUMENT;
     if (!a->scores || !a->argmax || !a->device_status || !a->workspace) return CLI_INVALID_ARGUMENT;
     if (!tape_ok(a->queries) || !tape_ok(a->documents)) return CLI_INVALID_ARGUMENT;
@@ -528,22 +544,26 @@ cli_status_t maxsim_scores(const cli_maxsim_t *a) {
     if (a->width > 256) return CLI_UNSUPPORTED;
     const size_t nq = a->queries.count, nd = a->documents.count, rq = a->queries.rows, rd = a->documents.rows;
     if (a->ld_scores < nd || a->ld_argmax < rq) return CLI_SHAPE_MISMATCH;
-    if (a->workspace_bytes < maxsim_workspace_bytes(nq, nd, rq, rd, a->width) || !aligned(a->workspace, 256))
-        return CLI_INVALID_ARGUMENT;
+    if (pairs && (!pairs->offsets || !edges_ok(*pairs))) return CLI_INVALID_ARGUMENT;
+    const size_t wsb = pairs ? maxsim_named_workspace_bytes(nq, nd, rq, rd, a->width)
+                             : maxsim_workspace_bytes(nq, nd, rq, rd, a->width);
+    if (a->workspace_bytes < wsb || !aligned(a->workspace, 256)) return CLI_INVALID_ARGUMENT;
     const Range inputs[] = {
         range_of(a->queries.data, rq * a->width * 2), range_of(a->queries.offsets, (nq + 1) * 8),
         range_of(a->documents.data, rd * a->width * 2), range_of(a->documents.offsets, (nd + 1) * 8),
+        pairs ? range_of(pairs->offsets, (nq + 1) * 8) : Range{0, 0},
+        pairs ? range_of(pairs->ids, pairs->edges * 4) : Range{0, 0},
     };
     const Range outputs[] = {
         range_of(a->scores, ((nq - 1) * a->ld_scores + nd) * 4),
         range_of(a->argmax, ((nd - 1) * a->ld_argmax + rq) * 4),
-        range_of(a->workspace, maxsim_workspace_bytes(nq, nd, rq, rd, a->width)),
+        range_of(a->workspace, wsb),
         range_of(a->device_status, 4),
     };
-    if (any_overlap(inputs, 4, outputs, 4)) return CLI_INVALID_ARGUMENT;
+    if (any_overlap(inputs, 6, outputs, 4)) return CLI_INVALID_ARGUMENT;
     const int sms = sm_count();
     if (sms <= 0) return CLI_DEVICE;
-    const MaxSimWs ws = carve_maxsim(a->workspace, nd, rq, rd, sms);
+    const MaxSimWs ws = carve_maxsim(a->workspace, nd, rq, rd, sms, pairs != nullptr);
     cudaStream_t stream = static_cast<cudaStream_t>(a->stream);
     CUtensorMap tq, td;
     if (!encode_bf16_rows(&tq, a->queries.data, a->width, rq, a->width) ||
@@ -572,8 +592,40 @@ cli_status_t maxsim_scores(const cli_maxsim_t *a) {
     L.chunk_rows = ws.chunk_rows;
     L.status = a->device_status;
     L.sm_count = sms;
+    if (pairs) {
+        // Pairs index documents; an argmax entry of a pair no query names is 0.
+        if (launch_validate_edges(to_set(*pairs), static_cast<int>(nq), static_cast<int>(nd), a->device_status,
+                                  stream) != cudaSuccess)
+            return CLI_DEVICE;
+        if (cudaMemset2DAsync(a->argmax, a->ld_argmax * 4, 0, rq * 4, nd, stream) != cudaSuccess) return CLI_DEVICE;
+        const size_t items = named_items_max(rq, rd);
+        uint8_t *q = static_cast<uint8_t *>(a->workspace) + ws.bytes;
+        L.pair_off = pairs->offsets;
+        L.pair_ids = pairs->ids;
+        L.item_flags = reinterpret_cast<uint32_t *>(q);
+        L.item_list = reinterpret_cast<uint32_t *>(q + align256(items * 4));
+        L.item_count = reinterpret_cast<uint32_t *>(q + 2 * align256(items * 4));
+    }
     if (launch_maxsim_forward(tq, td, L, stream) != cudaSuccess) return CLI_DEVICE;
     return CLI_OK;
+}
+
+}  // namespace
+}  // namespace cli
+
+extern "C" {
+
+cli_status_t maxsim_scores(const cli_maxsim_t *a) { return maxsim_forward_call(a, nullptr); }
+
+size_t maxsim_named_workspace_bytes(size_t query_count, size_t document_count, size_t query_rows,
+                                    size_t document_rows, size_t width) {
+    return maxsim_workspace_bytes(query_count, document_count, query_rows, document_rows, width) +
+           2 * align256(named_items_max(query_rows, document_rows) * 4) + 256;
+}
+
+cli_status_t maxsim_scores_named(const cli_maxsim_named_t *a) {
+    if (!a) return CLI_INVALID_ARGUMENT;
+    return maxsim_forward_call(&a->base, &a->pairs);
 }
 
 size_t maxsim_backward_workspace_bytes(size_t query_count, size_t document_count, size_t query_rows,

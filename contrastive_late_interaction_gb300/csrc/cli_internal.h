@@ -127,6 +127,13 @@ struct MaxSimLaunch {
     int n_chunks, chunk_rows;
     int32_t *status;
     int sm_count;
+    // Named pairs (pair_off null: every pair): the documents each query scores
+    // (CSR over the queries, validated), and workspace for the item schedule.
+    const uint64_t *pair_off = nullptr;
+    const uint32_t *pair_ids = nullptr;
+    uint32_t *item_flags = nullptr;   // [n_chunks * n_mblocks]
+    uint32_t *item_list = nullptr;    // [n_chunks * n_mblocks]
+    uint32_t *item_count = nullptr;   // [1]
 };
 cudaError_t launch_maxsim_forward(const CUtensorMap &tmap_q, const CUtensorMap &tmap_d, const MaxSimLaunch &L,
                                   cudaStream_t stream);

@@ -64,7 +64,20 @@ struct Params {
     long long ld_argmax;
     float *mval;
     int32_t *status;
+    // Named pairs: the work items to run (chunk * n_mblocks + mblock, in
+    // chunk-major order) and their count on the device; null runs every item.
+    const uint32_t *item_list, *item_count;
 };
+
+// The number of work items and the w-th one as (chunk, query block).
+__device__ __forceinline__ long long item_total(const Params &P) {
+    return P.item_list ? static_cast<long long>(*P.item_count) : P.items;
+}
+__device__ __forceinline__ void item_at(const Params &P, long long w, int &chunk, int &mb) {
+    const long long it = P.item_list ? static_cast<long long>(P.item_list[w]) : w;
+    chunk = static_cast<int>(it / P.n_mblocks);
+    mb = static_cast<int>(it % P.n_mblocks);
+}
 
 // Running (max, argmax) update from 32 scores of one chunk, restricted to
 // columns [lo, hi) of the chunk; `base` is the chunk's first row relative to
@@ -143,8 +156,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             int stage = 0;
             uint32_t phase = 0, it = 0;
             bool ok = true;
-            for (long long w = blockIdx.x; w < P.items && ok; w += gridDim.x) {
-                const int chunk = static_cast<int>(w / P.n_mblocks), mb = static_cast<int>(w % P.n_mblocks);
+            const long long items = item_total(P);
+            for (long long w = blockIdx.x; w < items && ok; w += gridDim.x) {
+                int chunk, mb;
+                item_at(P, w, chunk, mb);
                 const uint32_t d0 = P.chunk_doc[chunk], d1 = P.chunk_doc[chunk + 1];
                 if (d0 == d1) continue;
                 const long long r_lo = static_cast<long long>(P.d_off[d0]), r_hi = static_cast<long long>(P.d_off[d1]);
@@ -176,8 +191,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             int stage = 0;
             uint32_t phase = 0, it = 0, tc = 0;
             bool ok = true;
-            for (long long w = blockIdx.x; w < P.items && ok; w += gridDim.x) {
-                const int chunk = static_cast<int>(w / P.n_mblocks);
+            const long long items = item_total(P);
+            for (long long w = blockIdx.x; w < items && ok; w += gridDim.x) {
+                int chunk, mb;
+                item_at(P, w, chunk, mb);
+                (void)mb;
                 const uint32_t d0 = P.chunk_doc[chunk], d1 = P.chunk_doc[chunk + 1];
                 if (d0 == d1) continue;
                 const long long r_lo = static_cast<long long>(P.d_off[d0]), r_hi = static_cast<long long>(P.d_off[d1]);
@@ -215,8 +233,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         asm volatile("mov.b32 %0, 0xFFFFFFE0;" : "=r"(hi_mask));   // opaque to constant folding
         uint32_t tc = 0;
         bool ok = true;
-        for (long long w = blockIdx.x; w < P.items && ok; w += gridDim.x) {
-            const int chunk = static_cast<int>(w / P.n_mblocks), mb = static_cast<int>(w % P.n_mblocks);
+        const long long items = item_total(P);
+        for (long long w = blockIdx.x; w < items && ok; w += gridDim.x) {
+            int chunk, mb;
+            item_at(P, w, chunk, mb);
             const uint32_t d0 = P.chunk_doc[chunk], d1 = P.chunk_doc[chunk + 1];
             if (d0 == d1) continue;
             // Positions below are 32-bit offsets from the item's first row.
@@ -316,6 +336,68 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
+}
+
+// Named pairs: flags[chunk * n_mblocks + mb] = 1 for every work item holding a
+// (query, document) pair that some query names (one thread per query).
+__global__ void mark_items_kernel(const uint64_t *q_off, const uint64_t *pair_off, const uint32_t *pair_ids, int nq,
+                                  const uint32_t *chunk_doc, int n_chunks, int n_mblocks, uint32_t *flags,
+                                  const int32_t *status) {
+    if (read_status(status) != 0) return;
+    const int q = blockIdx.x * blockDim.x + threadIdx.x;
+    if (q >= nq) return;
+    const int mb0 = static_cast<int>(q_off[q] / 128), mb1 = static_cast<int>((q_off[q + 1] - 1) / 128);
+    for (uint64_t k = pair_off[q]; k < pair_off[q + 1]; ++k) {
+        const uint32_t d = pair_ids[k];
+        int lo = 0, hi = n_chunks;   // the chunk c with chunk_doc[c] <= d < chunk_doc[c + 1]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (chunk_doc[mid] <= d) lo = mid; else hi = mid;
+        }
+        for (int mb = mb0; mb <= mb1; ++mb) flags[static_cast<long long>(lo) * n_mblocks + mb] = 1u;
+    }
+}
+
+// The flagged items in index order (chunk-major) and their count: one block,
+// each thread compacting a contiguous segment after a scan of the counts.
+constexpr int kCompactThreads = 1024;
+__global__ void __launch_bounds__(kCompactThreads) compact_items_kernel(const uint32_t *flags, long long n,
+                                                                        uint32_t *list, uint32_t *count,
+                                                                        const int32_t *status) {
+    __shared__ uint32_t part[kCompactThreads];
+    if (read_status(status) != 0) return;
+    const long long per = (n + kCompactThreads - 1) / kCompactThreads;
+    const long long lo = threadIdx.x * per, hi = lo + per < n ? lo + per : n;
+    uint32_t c = 0;
+    for (long long i = lo; i < hi; ++i) c += flags[i] ? 1u : 0u;
+    part[threadIdx.x] = c;
+    __syncthreads();
+    for (int o = 1; o < kCompactThreads; o <<= 1) {   // inclusive scan (Hillis-Steele)
+        const uint32_t v = threadIdx.x >= o ? part[threadIdx.x - o] : 0u;
+        __syncthreads();
+        part[threadIdx.x] += v;
+        __syncthreads();
+    }
+    uint32_t at = part[threadIdx.x] - c;
+    for (long long i = lo; i < hi; ++i)
+        if (flags[i]) list[at++] = static_cast<uint32_t>(i);
+    if (threadIdx.x == kCompactThreads - 1) *count = part[threadIdx.x];
+}
+
+// S(q, d) = 0 for every pair no query names (one thread per cell).
+__global__ void mask_scores_kernel(const uint64_t *pair_off, const uint32_t *pair_ids, int nq, int nd, float *scores,
+                                   long long ld_scores, const int32_t *status) {
+    if (read_status(status) != 0) return;
+    const long long cell = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (cell >= static_cast<long long>(nq) * nd) return;
+    const int q = static_cast<int>(cell / nd), d = static_cast<int>(cell % nd);
+    uint64_t lo = pair_off[q], hi = pair_off[q + 1];
+    while (lo < hi) {
+        const uint64_t mid = (lo + hi) >> 1;
+        if (pair_ids[mid] < static_cast<uint32_t>(d)) lo = mid + 1; else hi = mid;
+    }
+    const bool named = lo < pair_off[q + 1] && pair_ids[lo] == static_cast<uint32_t>(d);
+    if (!named) scores[static_cast<long long>(q) * ld_scores + d] = 0.0f;
 }
 
 // chunk_doc[k] = first document starting at or after row k * chunk_rows;
@@ -563,6 +645,9 @@ __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch 
     const int32_t *am = L.argmax + static_cast<long long>(d) * L.ld_argmax;
     const bool use_table = L.nq <= kDsMaxTable;
     const bool packed = L.nq <= 65536;   // list entries carry the query as well as the row
+    // With c(q, d) in the shared table, rows whose c is zero (pairs a named loss does not score) are left out
+    // of the buckets: they add nothing.
+    const bool skip_zero = use_table && packed;
     if (use_table)
         for (int q = threadIdx.x; q < L.nq; q += kDsThreads) {
             float c = L.d_scores[static_cast<long long>(q) * L.ld_ds + d];
@@ -580,11 +665,12 @@ __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch 
             __syncthreads();
             // 1. histogram of the chunk's targets inside the window (eight loads in flight per thread)
             for (int k0 = threadIdx.x; k0 < crows; k0 += kDsBatch * kDsThreads) {
-                int a[kDsBatch];
+                int a[kDsBatch], qv[kDsBatch];
 #pragma unroll
                 for (int i = 0; i < kDsBatch; ++i) {
                     const int k = k0 + i * kDsThreads;
                     a[i] = k < crows ? __ldg(am + c0 + k) : 0;
+                    qv[i] = (skip_zero && k < crows) ? __ldg(L.qmap + c0 + k) : 0;
                 }
 #pragma unroll
                 for (int i = 0; i < kDsBatch; ++i) {
@@ -593,6 +679,7 @@ __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch 
                         report(L.status, CLI_MALFORMED);
                         continue;
                     }
+                    if (skip_zero && ctab[qv[i]] == 0.0f) continue;   // adds nothing to dD
                     const int r = a[i] - w0;
                     if (r >= 0 && r < wrows) atomicAdd(&cnt[r], 1u);
                 }
@@ -644,6 +731,7 @@ __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch 
 #pragma unroll
                 for (int i = 0; i < kDsBatch; ++i) {
                     const int r = a[i] - w0;
+                    if (skip_zero && a[i] >= 0 && ctab[qk[i] >> 16] == 0.0f) continue;   // as in the histogram
                     if (a[i] >= 0 && a[i] < dl && r >= 0 && r < wrows)
                         list[atomicAdd(&cnt[r], 1u)] = qk[i] | static_cast<uint32_t>(k0 + i * kDsThreads);
                 }
@@ -715,6 +803,20 @@ cudaError_t launch_maxsim_forward(const CUtensorMap &tmap_q, const CUtensorMap &
     P.ld_argmax = L.ld_argmax;
     P.mval = L.mval;
     P.status = L.status;
+    P.item_list = nullptr;
+    P.item_count = nullptr;
+    if (L.pair_off) {   // named pairs: run only the items that hold one
+        const long long n_items = P.items;
+        if ((err = cudaMemsetAsync(L.item_flags, 0, static_cast<size_t>(n_items) * 4, stream)) != cudaSuccess) return err;
+        mark_items_kernel<<<(L.nq + 255) / 256, 256, 0, stream>>>(L.q_off, L.pair_off, L.pair_ids, L.nq, L.chunk_doc,
+                                                                 L.n_chunks, P.n_mblocks, L.item_flags, L.status);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        compact_items_kernel<<<1, kCompactThreads, 0, stream>>>(L.item_flags, n_items, L.item_list, L.item_count,
+                                                                L.status);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        P.item_list = L.item_list;
+        P.item_count = L.item_count;
+    }
     // At least 80 KB so that no more than two CTAs (2 x 256 TMEM columns) share an SM.
     size_t smem = smem_bytes_for(P.nk);
     if (smem < 80 * 1024) smem = 80 * 1024;
@@ -732,6 +834,12 @@ cudaError_t launch_maxsim_forward(const CUtensorMap &tmap_q, const CUtensorMap &
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     query_sum_kernel<<<L.sm_count * 8, 256, 0, stream>>>(L.mval, L.q_off, L.nq, L.nd, L.rows_q, L.mean, L.scores,
                                                           L.ld_scores, L.status);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (L.pair_off) {
+        const long long cells = static_cast<long long>(L.nq) * L.nd;
+        mask_scores_kernel<<<static_cast<unsigned>((cells + 255) / 256), 256, 0, stream>>>(
+            L.pair_off, L.pair_ids, L.nq, L.nd, L.scores, L.ld_scores, L.status);
+    }
     return cudaGetLastError();
 }
 

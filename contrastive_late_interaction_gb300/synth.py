@@ -49,6 +49,7 @@ STREAM_SIDES = 9
 STREAM_WEIGHTS = 10
 STREAM_ARGMAX = 11
 STREAM_GROUPS = 12
+STREAM_NAMED = 13
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -347,3 +348,21 @@ def random_argmax(seed: int, mi: MaxSimInputs) -> np.ndarray:
     dl = np.diff(mi.d_offsets.astype(np.int64))
     u = uniform_closed0(seed, STREAM_ARGMAX, 0, mi.nd * rows_q).reshape(mi.nd, rows_q)
     return np.floor(u * dl[:, None]).astype(np.int32)
+
+
+def named_documents(seed: int, nq: int, nd: int, others: int) -> tuple[Edges, Edges]:
+    """Each query i names its own document i % nd (attract) and `others` further documents drawn uniformly
+    without replacement (repel).  Returns (attract, repel) as CSR edge sets over the queries."""
+    att, rep = [], []
+    for q in range(nq):
+        own = q % nd
+        draw = uniform_int(seed, STREAM_NAMED, others * 4, 0, nd - 1, start=q * others * 4)
+        picked = []
+        for d in draw.tolist():
+            if d != own and d not in picked:
+                picked.append(d)
+            if len(picked) == others:
+                break
+        att.append([own])
+        rep.append(sorted(picked))
+    return edges_from_lists(att), edges_from_lists(rep)

@@ -323,6 +323,32 @@ size_t maxsim_workspace_bytes(size_t query_count, size_t document_count, size_t 
                               size_t document_rows, size_t width);
 
 /*
+ * maxsim_scores_named -- hard MaxSim of each query against the documents it
+ * names only ("Training", `uform_late_interaction_side_t`: a query's tokens
+ * score the documents it attracts and repels, a document is scored by the
+ * queries naming it).  S(q, d) and the argmax of every named pair are those of
+ * maxsim_scores; for a pair no query names, S(q, d) = 0 and its argmax
+ * entries are row indices of the document (0 where its work item was skipped),
+ * so maxsim_backward runs on the same outputs (with dS = 0 there, as the
+ * named-negatives loss over S gives).  Work items (1024 document rows by 128
+ * query rows) that hold no named pair are not computed.
+ *
+ *   base      every field as in cli_maxsim_t; the workspace must hold
+ *             maxsim_named_workspace_bytes(...)
+ *   pairs     device CSR over the queries: offsets [count + 1], the documents
+ *             each query scores, strictly ascending, below documents.count
+ *             (CLI_MALFORMED in the device status otherwise); weights unread
+ */
+typedef struct {
+    cli_maxsim_t base;
+    cli_edges_t pairs;
+} cli_maxsim_named_t;
+
+cli_status_t maxsim_scores_named(const cli_maxsim_named_t *args);
+size_t maxsim_named_workspace_bytes(size_t query_count, size_t document_count, size_t query_rows,
+                                    size_t document_rows, size_t width);
+
+/*
  * maxsim_backward -- the gradient through the argmax: with
  * c = dS[q][d] (divided by |q| when mean), for every query token t of q,
  *     dQ[t]      += c * D[offsets_d + argmax[d][t]]

@@ -204,3 +204,21 @@ def test_groups_host_checks(b):
     assert f(groups=A * 7) == b.CLI_INVALID_ARGUMENT                     # an input inside the dE output
     assert f(count=3, d_bias=A * 8 + 8) == b.CLI_INVALID_ARGUMENT        # d_bias [3] overlaps d_inverse_temperature [3]
     assert f(count=3, embeddings=None) == b.CLI_INVALID_ARGUMENT         # the pooled checks still apply
+
+
+def test_maxsim_named_host_checks(b):
+    rq, rd, nq, nd, w = 4096, 65536, 100, 200, 128
+    ws = b.maxsim_named_workspace_bytes(nq, nd, rq, rd, w)
+    assert ws > b.maxsim_workspace_bytes(nq, nd, rq, rd, w)
+
+    def f(pairs=None, **o):
+        pairs = pairs if pairs is not None else b.Edges(A * 10, A * 11, None, 800)
+        args = b.MaxSimNamedArgs(base=maxsim_args(b, **{"workspace_bytes": ws, **o}), pairs=pairs)
+        return b.lib.maxsim_scores_named(ctypes.byref(args))
+
+    assert b.lib.maxsim_scores_named(None) == b.CLI_INVALID_ARGUMENT
+    assert f(pairs=b.Edges(None, None, None, 0)) == b.CLI_INVALID_ARGUMENT          # no pair list
+    assert f(pairs=b.Edges(A * 10, None, None, 800)) == b.CLI_INVALID_ARGUMENT      # ids missing
+    assert f(workspace_bytes=b.maxsim_workspace_bytes(nq, nd, rq, rd, w)) == b.CLI_INVALID_ARGUMENT
+    assert f(pairs=b.Edges(A * 5, A * 11, None, 800)) == b.CLI_INVALID_ARGUMENT     # offsets inside the scores
+    assert f(width=12) == b.CLI_SHAPE_MISMATCH                                        # the plain checks still apply
