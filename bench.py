@@ -263,8 +263,10 @@ class Step:
                 n += 3                                    # fused block kernel, two-level final reduction
         if self.m is not None:
             n += 2 + 1 + 1 + 1                            # 2 tape validations, schedule, forward, query sums
-            n += 2 + 1 + 1 + 1                            # 2 tape validations, row->query map, dQ, dD
+            if not self.named:
+                n += 2 + 1 + 1 + 1                        # 2 tape validations, row->query map, dQ, dD
             if self.named:
+                n += 2 + 1 + 1                            # 2 tape validations, pair validation, named backward
                 n += 1 + 1 + 1 + 1                        # pair validation, item marks, compaction, score mask
                 n += 2 + 1 + 1                            # 2 edge validations, score loss, final reduction
             if self.j is not None:
@@ -320,8 +322,12 @@ class Step:
                 else:
                     ds = self.ds
                 rec("maxsim_bwd", 0)
-                cli.maxsim_backward(self.q, self.qo, self.d, self.do, f["argmax"], ds, out=self.b_out,
-                                    workspace=self.b_ws, device_status=self.b_st, stream=self.stream)
+                if self.named:
+                    cli.maxsim_backward_named(self.q, self.qo, self.d, self.do, f["argmax"], ds, self.pairs,
+                                              out=self.b_out, device_status=self.b_st, stream=self.stream)
+                else:
+                    cli.maxsim_backward(self.q, self.qo, self.d, self.do, f["argmax"], ds, out=self.b_out,
+                                        workspace=self.b_ws, device_status=self.b_st, stream=self.stream)
                 rec("maxsim_bwd", 1)
 
     def upload(self):
@@ -632,7 +638,7 @@ def main():
         tf = (maxsim_fwd_flops(m, w.get("named")) + maxsim_bwd_flops(m, w.get("named"))) / ((fm + bm) * 1e-3) / 1e12
         parts["maxsim"] = {"fwd_ms": fm, "bwd_ms": bm, "tflops_fwd_bwd": tf, "frac_of_peak": tf / sustained,
                            "fwd_tflops": maxsim_fwd_flops(m, w.get("named")) / (fm * 1e-3) / 1e12,
-                           "bwd_gathered_gb_per_s": 2 * 2.0 * m.width * float(m.q_offsets[-1]) * m.nd / (bm * 1e-3) / 1e9}
+                           "bwd_gathered_gb_per_s": maxsim_bwd_flops(m, w.get("named")) / (bm * 1e-3) / 1e9}
         if step.j is not None or step.named is not None:
             parts["score_loss"] = {"ms": statistics.mean(part_ms["score_loss"])}
 

@@ -134,6 +134,10 @@ class MaxSimBackwardArgs(ctypes.Structure):
                 ("workspace_bytes", c_size_t), ("device_status", c_void_p), ("stream", c_void_p)]
 
 
+class MaxSimBackwardNamedArgs(ctypes.Structure):
+    _fields_ = [("base", MaxSimBackwardArgs), ("pairs", Edges)]
+
+
 EXPORTS = {
     "cli_status_name": (ctypes.c_char_p, [c_int]),
     "pair_loss_sigmoid_fwd_bwd": (c_int, [ctypes.POINTER(PairLossSigmoidArgs)]),
@@ -150,6 +154,7 @@ EXPORTS = {
     "maxsim_scores_named": (c_int, [ctypes.POINTER(MaxSimNamedArgs)]),
     "maxsim_named_workspace_bytes": (c_size_t, [c_size_t, c_size_t, c_size_t, c_size_t, c_size_t]),
     "maxsim_backward": (c_int, [ctypes.POINTER(MaxSimBackwardArgs)]),
+    "maxsim_backward_named": (c_int, [ctypes.POINTER(MaxSimBackwardNamedArgs)]),
     "maxsim_backward_workspace_bytes": (c_size_t, [c_size_t, c_size_t, c_size_t, c_size_t, c_size_t]),
     "maxsim_backward_no_alloc": (c_int, [ctypes.POINTER(MaxSimBackwardArgs)]),
 }
@@ -503,4 +508,26 @@ def maxsim_backward(q_data, q_offsets, d_data, d_offsets, argmax, d_scores, mean
                               d_queries=_ptr(dq), d_documents=_ptr(dd), workspace=_ptr(ws),
                               workspace_bytes=ws.numel(), device_status=_ptr(st), stream=_stream(stream))
     raise_for(lib.maxsim_backward(ctypes.byref(args)), "maxsim_backward")
+    return dict(d_queries=dq, d_documents=dd, device_status=st)
+
+
+def maxsim_backward_named(q_data, q_offsets, d_data, d_offsets, argmax, d_scores, pairs, mean=False, out=None,
+                          device_status=None, stream=None):
+    """Gradient through the argmax of the named pairs only (`pairs` as for maxsim_scores_named).  Returns
+    dict(d_queries, d_documents, device_status)."""
+    Q, D = _tape(q_data, q_offsets), _tape(d_data, d_offsets)
+    _check_cuda(argmax, "argmax", torch.int32)
+    _check_cuda(d_scores, "d_scores", torch.float32)
+    width = q_data.shape[1]
+    dev = q_data.device
+    out = dict(out or {})
+    dq = out.get("d_queries") if out.get("d_queries") is not None else torch.empty(Q.rows, width, device=dev)
+    dd = out.get("d_documents") if out.get("d_documents") is not None else torch.empty(D.rows, width, device=dev)
+    st = device_status if device_status is not None else torch.zeros(1, dtype=torch.int32, device=dev)
+    base = MaxSimBackwardArgs(queries=Q, documents=D, width=width, mean=int(bool(mean)), argmax=_ptr(argmax),
+                              ld_argmax=argmax.stride(0), d_scores=_ptr(d_scores), ld_d_scores=d_scores.stride(0),
+                              d_queries=_ptr(dq), d_documents=_ptr(dd), workspace=None, workspace_bytes=0,
+                              device_status=_ptr(st), stream=_stream(stream))
+    args = MaxSimBackwardNamedArgs(base=base, pairs=_edges(pairs, Q.count))
+    raise_for(lib.maxsim_backward_named(ctypes.byref(args)), "maxsim_backward_named")
     return dict(d_queries=dq, d_documents=dd, device_status=st)

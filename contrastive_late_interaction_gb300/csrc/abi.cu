@@ -637,23 +637,32 @@ size_t maxsim_backward_workspace_bytes(size_t query_count, size_t document_count
     return align256(query_rows * sizeof(int32_t));
 }
 
-cli_status_t maxsim_backward(const cli_maxsim_backward_t *a) {
+}  // extern "C"
+
+namespace cli {
+namespace {
+
+// maxsim_backward over every pair (pairs null) or the named ones only.
+cli_status_t maxsim_backward_call(const cli_maxsim_backward_t *a, const cli_edges_t *pairs) {
     if (!a) return CLI_INVALID_ARGUMENT;
-    if (!a->argmax || !a->d_scores || !a->d_queries || !a->d_documents || !a->device_status || !a->workspace)
-        return CLI_INVALID_ARGUMENT;
+    if (!a->argmax || !a->d_scores || !a->d_queries || !a->d_documents || !a->device_status) return CLI_INVALID_ARGUMENT;
+    if (!pairs && !a->workspace) return CLI_INVALID_ARGUMENT;
     if (!tape_ok(a->queries) || !tape_ok(a->documents)) return CLI_INVALID_ARGUMENT;
     if (a->width == 0 || a->width % 8 != 0) return CLI_SHAPE_MISMATCH;
     if (a->width > 256) return CLI_UNSUPPORTED;
     const size_t nq = a->queries.count, nd = a->documents.count, rq = a->queries.rows, rd = a->documents.rows;
     if (a->ld_d_scores < nd || a->ld_argmax < rq) return CLI_SHAPE_MISMATCH;
     if (!aligned(a->d_queries, 16) || !aligned(a->d_documents, 16)) return CLI_INVALID_ARGUMENT;
-    const size_t wsb = maxsim_backward_workspace_bytes(nq, nd, rq, rd, a->width);
-    if (a->workspace_bytes < wsb || !aligned(a->workspace, 256)) return CLI_INVALID_ARGUMENT;
+    if (pairs && (!pairs->offsets || !edges_ok(*pairs))) return CLI_INVALID_ARGUMENT;
+    const size_t wsb = pairs ? 0 : maxsim_backward_workspace_bytes(nq, nd, rq, rd, a->width);
+    if (!pairs && (a->workspace_bytes < wsb || !aligned(a->workspace, 256))) return CLI_INVALID_ARGUMENT;
     const Range inputs[] = {
         range_of(a->queries.data, rq * a->width * 2), range_of(a->queries.offsets, (nq + 1) * 8),
         range_of(a->documents.data, rd * a->width * 2), range_of(a->documents.offsets, (nd + 1) * 8),
         range_of(a->argmax, ((nd - 1) * a->ld_argmax + rq) * 4),
         range_of(a->d_scores, ((nq - 1) * a->ld_d_scores + nd) * 4),
+        pairs ? range_of(pairs->offsets, (nq + 1) * 8) : Range{0, 0},
+        pairs ? range_of(pairs->ids, pairs->edges * 4) : Range{0, 0},
     };
     const Range outputs[] = {
         range_of(a->d_queries, rq * a->width * 4),
@@ -661,7 +670,7 @@ cli_status_t maxsim_backward(const cli_maxsim_backward_t *a) {
         range_of(a->workspace, wsb),
         range_of(a->device_status, 4),
     };
-    if (any_overlap(inputs, 6, outputs, 4)) return CLI_INVALID_ARGUMENT;
+    if (any_overlap(inputs, 8, outputs, 4)) return CLI_INVALID_ARGUMENT;
     const int sms = sm_count();
     if (sms <= 0) return CLI_DEVICE;
     cudaStream_t stream = static_cast<cudaStream_t>(a->stream);
@@ -689,8 +698,32 @@ cli_status_t maxsim_backward(const cli_maxsim_backward_t *a) {
     L.qmap = static_cast<int32_t *>(a->workspace);
     L.status = a->device_status;
     L.sm_count = sms;
+    if (pairs) {
+        if (launch_validate_edges(to_set(*pairs), static_cast<int>(nq), static_cast<int>(nd), a->device_status,
+                                  stream) != cudaSuccess)
+            return CLI_DEVICE;
+        if (cudaMemsetAsync(a->d_queries, 0, rq * a->width * 4, stream) != cudaSuccess ||
+            cudaMemsetAsync(a->d_documents, 0, rd * a->width * 4, stream) != cudaSuccess)
+            return CLI_DEVICE;
+        if (launch_maxsim_backward_named(L, pairs->offsets, pairs->ids, static_cast<long long>(pairs->edges), stream) !=
+            cudaSuccess)
+            return CLI_DEVICE;
+        return CLI_OK;
+    }
     if (launch_maxsim_backward(L, stream) != cudaSuccess) return CLI_DEVICE;
     return CLI_OK;
+}
+
+}  // namespace
+}  // namespace cli
+
+extern "C" {
+
+cli_status_t maxsim_backward(const cli_maxsim_backward_t *a) { return maxsim_backward_call(a, nullptr); }
+
+cli_status_t maxsim_backward_named(const cli_maxsim_backward_named_t *a) {
+    if (!a) return CLI_INVALID_ARGUMENT;
+    return maxsim_backward_call(&a->base, &a->pairs);
 }
 
 }  // extern "C"

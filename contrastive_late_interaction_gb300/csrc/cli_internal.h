@@ -153,6 +153,9 @@ struct MaxSimBwdLaunch {
     int sm_count;
 };
 cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream);
+// The backward over named pairs only (dQ and dD zeroed by the caller).
+cudaError_t launch_maxsim_backward_named(const MaxSimBwdLaunch &L, const uint64_t *pair_off, const uint32_t *pair_ids,
+                                         long long pairs, cudaStream_t stream);
 
 // bf16 [rows x cols] (row stride ld elements) as a TMA map with boxes of
 // box_cols x box_rows, optionally with the 128-byte swizzle; out-of-range

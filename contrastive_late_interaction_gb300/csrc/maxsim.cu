@@ -774,6 +774,48 @@ __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch 
     }
 }
 
+// Backward over named pairs only: one warp per named (query, document) pair,
+// rows of the query in turn; lanes own 4 features of each 128-feature block.
+// dQ[t] += c D[argmax], dD[argmax] += c Q[t] with vector L2 reductions (dQ and
+// dD zeroed before): the sums reproduce to rounding, not bit for bit.
+__global__ void __launch_bounds__(256) named_backward_kernel(MaxSimBwdLaunch L, const uint64_t *pair_off,
+                                                             const uint32_t *pair_ids, long long pairs) {
+    if (read_status(L.status) != 0) return;
+    const long long k = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (k >= pairs) return;
+    int lo = 0, hi = L.nq;   // the query q with pair_off[q] <= k < pair_off[q + 1]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pair_off[mid] <= static_cast<uint64_t>(k)) lo = mid; else hi = mid;
+    }
+    const int q = lo, d = static_cast<int>(pair_ids[k]);
+    const uint64_t t0 = L.q_off[q], t1 = L.q_off[q + 1], o = L.d_off[d], len = L.d_off[d + 1] - o;
+    float c = L.d_scores[static_cast<long long>(q) * L.ld_ds + d];
+    if (L.mean) c /= static_cast<float>(t1 - t0);
+    if (c == 0.0f) return;
+    for (uint64_t t = t0; t < t1; ++t) {
+        const int a = __ldg(L.argmax + static_cast<long long>(d) * L.ld_argmax + static_cast<long long>(t));
+        if (a < 0 || static_cast<uint64_t>(a) >= len) {
+            if (lane == 0) report(L.status, CLI_MALFORMED);
+            continue;
+        }
+        const uint16_t *dr = L.d + (o + static_cast<uint64_t>(a)) * L.width, *qr = L.q + t * L.width;
+        float *dq = L.dq + t * L.width, *dd = L.dd + (o + static_cast<uint64_t>(a)) * L.width;
+        for (int f = lane * 4; f < L.width; f += 128) {
+            const uint2 xd = *reinterpret_cast<const uint2 *>(dr + f), xq = *reinterpret_cast<const uint2 *>(qr + f);
+            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dq + f),
+                         "f"(c * __uint_as_float(xd.x << 16)), "f"(c * __uint_as_float(xd.x & 0xFFFF0000u)),
+                         "f"(c * __uint_as_float(xd.y << 16)), "f"(c * __uint_as_float(xd.y & 0xFFFF0000u))
+                         : "memory");
+            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dd + f),
+                         "f"(c * __uint_as_float(xq.x << 16)), "f"(c * __uint_as_float(xq.x & 0xFFFF0000u)),
+                         "f"(c * __uint_as_float(xq.y << 16)), "f"(c * __uint_as_float(xq.y & 0xFFFF0000u))
+                         : "memory");
+        }
+    }
+}
+
 }  // namespace ms
 
 size_t maxsim_forward_smem_bytes(int width) { return ms::smem_bytes_for((width + ms::BK - 1) / ms::BK); }
@@ -868,6 +910,18 @@ cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream
             return err;
         dd_sort_kernel<2, 1><<<L.nd, kDsThreads, ds_smem, stream>>>(L);
     }
+    return cudaGetLastError();
+}
+
+}  // namespace cli
+
+namespace cli {
+
+cudaError_t launch_maxsim_backward_named(const MaxSimBwdLaunch &L, const uint64_t *pair_off, const uint32_t *pair_ids,
+                                         long long pairs, cudaStream_t stream) {
+    if (pairs == 0) return cudaSuccess;
+    ms::named_backward_kernel<<<static_cast<unsigned>((pairs + 7) / 8), 256, 0, stream>>>(L, pair_off, pair_ids,
+                                                                                        pairs);
     return cudaGetLastError();
 }
 

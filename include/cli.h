@@ -380,6 +380,24 @@ size_t maxsim_backward_workspace_bytes(size_t query_count, size_t document_count
                                        size_t document_rows, size_t width);
 
 /*
+ * maxsim_backward_named -- the MaxSim backward over the named pairs only (the
+ * pairs of maxsim_scores_named): dQ and dD receive c(q, d) Q/D rows through the
+ * argmax of every named pair, and a pair no query names contributes nothing,
+ * whatever dS holds there.  One warp per named pair adds its rows into dQ and
+ * dD with vector L2 reductions, so dQ and dD reproduce to rounding, not bit
+ * for bit.  The workspace is not used (base.workspace may be NULL).
+ *
+ *   base      every other field as in cli_maxsim_backward_t
+ *   pairs     as in cli_maxsim_named_t
+ */
+typedef struct {
+    cli_maxsim_backward_t base;
+    cli_edges_t pairs;
+} cli_maxsim_backward_named_t;
+
+cli_status_t maxsim_backward_named(const cli_maxsim_backward_named_t *args);
+
+/*
  * maxsim_backward_no_alloc -- maxsim_backward for callers that cannot allocate
  * device memory and have no buffer to lend as workspace: code running where an
  * allocation is not allowed or would stall the device, or a runtime whose

@@ -222,3 +222,22 @@ def test_maxsim_named_host_checks(b):
     assert f(workspace_bytes=b.maxsim_workspace_bytes(nq, nd, rq, rd, w)) == b.CLI_INVALID_ARGUMENT
     assert f(pairs=b.Edges(A * 5, A * 11, None, 800)) == b.CLI_INVALID_ARGUMENT     # offsets inside the scores
     assert f(width=12) == b.CLI_SHAPE_MISMATCH                                        # the plain checks still apply
+
+
+def test_maxsim_backward_named_host_checks(b):
+    rq, rd, nq, nd, w = 4096, 65536, 100, 200, 128
+
+    def f(pairs=None, **o):
+        pairs = pairs if pairs is not None else b.Edges(A * 10, A * 11, None, 800)
+        args = dict(queries=b.Tape(A * 1, A * 2, nq, rq), documents=b.Tape(A * 3, A * 4, nd, rd), width=w, mean=0,
+                    argmax=A * 5, ld_argmax=rq, d_scores=A * 6, ld_d_scores=nd, d_queries=A * 7, d_documents=A * 8,
+                    workspace=None, workspace_bytes=0, device_status=A * 9, stream=None)
+        args.update(o)
+        named = b.MaxSimBackwardNamedArgs(base=b.MaxSimBackwardArgs(**args), pairs=pairs)
+        return b.lib.maxsim_backward_named(ctypes.byref(named))
+
+    assert b.lib.maxsim_backward_named(None) == b.CLI_INVALID_ARGUMENT
+    assert f(pairs=b.Edges(None, None, None, 0)) == b.CLI_INVALID_ARGUMENT
+    assert f(d_queries=A * 7 + 4) == b.CLI_INVALID_ARGUMENT                       # misaligned output
+    assert f(pairs=b.Edges(A * 7, A * 11, None, 800)) == b.CLI_INVALID_ARGUMENT    # pair offsets inside dQ
+    assert f(width=264) == b.CLI_UNSUPPORTED

@@ -100,3 +100,25 @@ def test_a_pair_past_the_documents_is_malformed():
     lists[4] = [1, 12]
     r = run_named(m, lists)
     assert cli.status_name(int(r["device_status"].item())) == "malformed"
+
+
+@pytest.mark.parametrize("mean", [False, True])
+def test_named_backward_ignores_pairs_not_named(mean):
+    """maxsim_backward_named with a dS that is nonzero everywhere: only the named pairs reach dQ and dD."""
+    import contrastive_late_interaction_gb300 as cli
+    m = synth.maxsim_random(25, 50, 70, 128, (2, 70), (3, 260))
+    lists = named_lists(4, m.nq, m.nd, 1, 6)
+    pairs = cli.device_edges(synth.edges_from_lists(lists))
+    f = cli.maxsim_scores_named(bf16(m.q_bf16), i64(m.q_offsets), bf16(m.d_bf16), i64(m.d_offsets), pairs, mean=mean)
+    g = cli.maxsim_backward_named(bf16(m.q_bf16), i64(m.q_offsets), bf16(m.d_bf16), i64(m.d_offsets), f["argmax"],
+                                  torch.from_numpy(np.ascontiguousarray(m.d_scores)).to(dev()), pairs, mean=mean)
+    torch.cuda.synchronize()
+    assert int(f["device_status"].item()) == 0 and int(g["device_status"].item()) == 0
+    named = np.zeros((m.nq, m.nd), bool)
+    for q, docs in enumerate(lists):
+        named[q, docs] = True
+    _, arg, _ = oracle.maxsim_forward(m.q_offsets, m.q, m.d_offsets, m.d)
+    ds = np.where(named, m.d_scores, 0.0)
+    dq, dd = oracle.maxsim_backward(m.q_offsets, m.q, m.d_offsets, m.d, arg, ds, mean)
+    assert rel_l2(g["d_queries"].double().cpu().numpy(), dq) <= GRAD_RL2
+    assert rel_l2(g["d_documents"].double().cpu().numpy(), dd) <= GRAD_RL2
