@@ -469,7 +469,9 @@ __device__ __forceinline__ void fma_bf16x8(float2 (&acc)[4], const uint4 u, floa
 constexpr int kDqRows = 32;
 constexpr int kDqUnroll = 8;
 template <int NBLK>   // 64-feature blocks of the width (1..4)
-__global__ void __launch_bounds__(256) dq_kernel(MaxSimBwdLaunch L) {
+// Up to width 128, at most 64 registers, so four blocks (32 warps) share an SM: the gathers are
+// latency-bound.
+__global__ void __launch_bounds__(256, NBLK <= 2 ? 4 : 2) dq_kernel(MaxSimBwdLaunch L) {
     if (read_status(L.status) != 0) return;
     const int t = blockIdx.x * kDqRows + (threadIdx.x >> 3);
     const int sub = threadIdx.x & 7;
