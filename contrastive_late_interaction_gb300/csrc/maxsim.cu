@@ -498,14 +498,15 @@ __global__ void __launch_bounds__(256, NBLK <= 2 ? 4 : 2) dq_kernel(MaxSimBwdLau
             c_n = __ldg(dsrow + d);
         }
     };
-    // ... and their use: the gathered row (0 past the last document or for a rejected entry) and c.
+    // ... and their use: the gathered row (0 past the last document, for a rejected entry or for c = 0)
+    // and c.
     auto finish = [&](int d, unsigned long long &src, float &c) {
         src = 0;
         c = 0.f;
         if (d < L.nd) {
             if (a_n < 0 || static_cast<uint64_t>(a_n) >= e_n - o_n) {
                 if (row_ok) report(L.status, CLI_MALFORMED);
-            } else {
+            } else if (c_n != 0.0f) {   // a pair with c = 0 (one a loss ignores) gathers nothing
                 src = reinterpret_cast<unsigned long long>(L.d + (o_n + static_cast<uint64_t>(a_n)) * L.width);
                 c = c_n * scale;
             }
