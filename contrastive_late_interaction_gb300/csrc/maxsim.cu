@@ -12,10 +12,13 @@
 // tiles back, one query row per thread, and keep a running (max, argmax) per
 // row across the tiles of the current document; the boundaries between
 // documents are the same for every row, so the segment logic is warp-uniform.
-// The max over a 32-column chunk is a tree of float max operations on keys that
-// carry the column in the 5 low mantissa bits (31 - column, so equal values
-// resolve to the lowest column), which costs about two instructions per cell;
-// the value it reports is truncated by less than 2^-18 relative.
+// Per 32-column chunk each score becomes a key that carries the column in the
+// 5 low mantissa bits (31 - column, so equal values resolve to the lowest
+// column; one ALU instruction per cell).  For a chunk inside one document the
+// keys go back into TMEM and a reducing TMEM load returns their maximum; a
+// chunk holding a document boundary masks its keys per segment and reduces
+// them with a tree of three-input max operations.  The reported value is
+// truncated by less than 2^-18 relative.
 //
 // The ragged schedule: the document tape is cut into chunks of whole
 // documents of about `chunk_rows` rows (a binary search over the offsets per
@@ -79,14 +82,115 @@ __device__ __forceinline__ void item_at(const Params &P, long long w, int &chunk
     mb = static_cast<int>(it % P.n_mblocks);
 }
 
-// Running (max, argmax) update from 32 scores of one chunk, restricted to
-// columns [lo, hi) of the chunk; `base` is the chunk's first row relative to
-// the current document.  Keys carry 31 - column in the 5 low mantissa bits, so
-// the max of the keys names the lowest column among equal values; the tree
-// uses the three-input max (16 instructions for 32 keys).
-// Each key is (bits & hi_mask) | (31 - r), one lop3 with the mask (~31) held
-// in a register so the two-constant form does not split into two operations.
-template <bool kFull>
+// Keys: each score's bits with the 5 low mantissa bits replaced by 31 - column
+// (one lop3, the mask ~31 held in a register so the two-constant form does not
+// split into two operations).  The largest key is the largest score truncated
+// by less than 2^-18 relative, and among equal truncated scores it names the
+// lowest column.
+
+// Running (max, argmax) update from the largest key of a chunk's columns of the
+// current document; `base` is the chunk's first row relative to the document.
+__device__ __forceinline__ void update_best(float key, int base, float &best, int &best_col) {
+    const int bits = __float_as_int(key);
+    const float val = __int_as_float(bits & ~31);
+    if (val > best) {
+        best = val;
+        best_col = base + (31 - (bits & 31));
+    }
+}
+
+// The keys of a chunk into TMEM (over its scores, which are not read again).
+__device__ __forceinline__ void chunk_keys_to_tmem(uint32_t taddr, uint32_t hi_mask) {
+    uint32_t r[32];
+    tmem_ld32_async(taddr, r);
+    tmem_wait_ld();
+    tmem_regs_ready(r);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r[i]) : "r"(r[i]), "r"(hi_mask), "r"(31 - i));
+    tmem_st32(taddr, r);
+    tmem_wait_st();
+    tmem_regs_ready(r);   // the store's registers stay reserved until it has completed
+}
+
+// The update from a chunk wholly inside the current document: its keys go to
+// TMEM and a reducing TMEM load returns their maximum, so no max tree runs on
+// the ALU.
+__device__ __forceinline__ void chunk_max_tmem(uint32_t taddr, int base, float &best, int &best_col,
+                                               uint32_t hi_mask) {
+    chunk_keys_to_tmem(taddr, hi_mask);
+    uint32_t x[32];
+    float m;
+    tmem_ld32_max_async(taddr, x, m);
+    tmem_wait_ld();
+    tmem_regs_ready(x, m);
+    update_best(m, base, best, best_col);
+}
+
+// Largest keys of a chunk's columns [0, p) and [p, 32) (0 < p < 32, warp-uniform)
+// from keys already in TMEM.  Each range is a run of aligned power-of-two
+// pieces (the prefix by the bits of p from the top, the suffix by the bits of
+// p from the bottom).  Every piece slot is loaded, an absent one from the
+// chunk's first columns, and dropped afterwards, so no register written by an
+// asynchronous load is merged across a branch; all loads are in flight
+// together, and the TMEM loads reduce the pieces of four columns and more.
+struct SplitLoads {
+    uint32_t r16[16], r8[8], r4[4], r2[2], r1;
+    float m16, m8, m4;
+    unsigned present;   // bit s: the piece of 2^s columns is part of the range
+};
+
+__device__ __forceinline__ void split_issue(uint32_t ta, int lo_of[5], SplitLoads &x) {
+    auto at = [&](int s) { return ta + static_cast<uint32_t>((x.present >> s) & 1u ? lo_of[s] : 0); };
+    tmem_ld16_max_async(at(4), x.r16, x.m16);
+    tmem_ld8_max_async(at(3), x.r8, x.m8);
+    tmem_ld4_max_async(at(2), x.r4, x.m4);
+    tmem_ld2_async(at(1), x.r2);
+    tmem_ld1_async(at(0), x.r1);
+}
+
+__device__ __forceinline__ float split_result(SplitLoads &x) {
+    tmem_regs_ready_n(x.r16);
+    tmem_regs_ready_n(x.r8);
+    tmem_regs_ready_n(x.r4);
+    tmem_regs_ready_n(x.r2);
+    asm volatile("" : "+r"(x.r1), "+f"(x.m16), "+f"(x.m8), "+f"(x.m4)::"memory");
+    const float ninf = -INFINITY;
+    const unsigned pr = x.present;
+    const float m2 = fmaxf(__uint_as_float(x.r2[0]), __uint_as_float(x.r2[1]));
+    return fmaxf(fmax3(pr & 16u ? x.m16 : ninf, pr & 8u ? x.m8 : ninf, pr & 4u ? x.m4 : ninf),
+                 fmaxf(pr & 2u ? m2 : ninf, pr & 1u ? __uint_as_float(x.r1) : ninf));
+}
+
+// `two`: whether the suffix is wanted.
+__device__ __forceinline__ void split_max(uint32_t ta, int p, bool two, float &ma, float &mb) {
+    SplitLoads a, b;
+    int lo_a[5], lo_b[5];
+    a.present = static_cast<unsigned>(p) & 31u;   // prefix: pieces from the largest down
+    int lo = 0;
+#pragma unroll
+    for (int s = 4; s >= 0; --s) {
+        lo_a[s] = lo;
+        if (a.present & (1u << s)) lo += 1 << s;
+    }
+    b.present = two ? (32u - static_cast<unsigned>(p)) & 31u : 0u;   // suffix: from the smallest up
+    lo = p;
+#pragma unroll
+    for (int s = 0; s < 5; ++s) {
+        lo_b[s] = lo;
+        if (b.present & (1u << s)) lo += 1 << s;
+    }
+    split_issue(ta, lo_a, a);
+    split_issue(ta, lo_b, b);
+    tmem_wait_ld();
+    ma = split_result(a);
+    mb = split_result(b);
+}
+
+// The update from 32 scores of a chunk restricted to its columns [lo, hi)
+// (a chunk holding a document boundary or the end of the work item): keys
+// outside the range become -inf and a tree of three-input max operations
+// (16 instructions) picks the largest.
 __device__ __forceinline__ void chunk_max(const float (&v)[32], int lo, int hi, int base, float &best, int &best_col,
                                           uint32_t hi_mask) {
     float key[32];
@@ -94,8 +198,7 @@ __device__ __forceinline__ void chunk_max(const float (&v)[32], int lo, int hi, 
     for (int r = 0; r < 32; ++r) {
         uint32_t kb;
         asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(kb) : "r"(__float_as_uint(v[r])), "r"(hi_mask), "r"(31 - r));
-        const float k = __uint_as_float(kb);
-        key[r] = kFull ? k : ((r >= lo && r < hi) ? k : -INFINITY);
+        key[r] = (r >= lo && r < hi) ? __uint_as_float(kb) : -INFINITY;
     }
     float m[12];
 #pragma unroll
@@ -104,13 +207,7 @@ __device__ __forceinline__ void chunk_max(const float (&v)[32], int lo, int hi, 
     m[11] = key[31];
     const float n0 = fmax3(m[0], m[1], m[2]), n1 = fmax3(m[3], m[4], m[5]);
     const float n2 = fmax3(m[6], m[7], m[8]), n3 = fmax3(m[9], m[10], m[11]);
-    const float top = fmaxf(fmax3(n0, n1, n2), n3);
-    const int bits = __float_as_int(top);
-    const float val = __int_as_float(bits & ~31);
-    if (val > best) {
-        best = val;
-        best_col = base + (31 - (bits & 31));
-    }
+    update_best(fmaxf(fmax3(n0, n1, n2), n3), base, best, best_col);
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
@@ -248,6 +345,20 @@ __global__ void __launch_bounds__(kThreads, 2)
             int cur_beg = 0, cur_end = static_cast<int>(static_cast<long long>(P.d_off[d0 + 1]) - r_lo);
             float best = -INFINITY;
             int best_col = 0;
+            // The current document is complete: its row maximum and argmax out, the next one begins.
+            auto close_doc = [&]() {
+                if (t_ok) {
+                    P.argmax[static_cast<long long>(cur) * P.ld_argmax + t] = best_col;
+                    P.mval[static_cast<long long>(cur) * P.rows_q + t] = best;
+                }
+                ++cur;
+                best = -INFINITY;
+                best_col = 0;
+                if (cur < d1) {
+                    cur_beg = cur_end;
+                    cur_end = static_cast<int>(static_cast<long long>(P.d_off[cur + 1]) - r_lo);
+                }
+            };
             for (int r0 = 0; r0 < span; r0 += BN, ++tc) {
                 const uint32_t buf = tc & 1;
                 if (!mbar_wait(&bar.s_full[buf], (tc >> 1) & 1, abort_flag, P.status, kSleepEpilogue)) { ok = false; break; }
@@ -255,24 +366,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (r0 + BN <= span && cur_end >= r0 + BN) {
                     // the whole tile lies inside the current document
 #pragma unroll 1
-                    for (int ch = 0; ch < BN / 32; ++ch) {
-                        float v[32];
-                        tmem_ld32(tmem + lane_base + buf * BN + ch * 32, v);
-                        chunk_max<true>(v, 0, 32, r0 + ch * 32 - cur_beg, best, best_col, hi_mask);
-                    }
-                    if (cur_end == r0 + BN) {
-                        if (t_ok) {
-                            P.argmax[static_cast<long long>(cur) * P.ld_argmax + t] = best_col;
-                            P.mval[static_cast<long long>(cur) * P.rows_q + t] = best;
-                        }
-                        ++cur;
-                        best = -INFINITY;
-                        best_col = 0;
-                        if (cur < d1) {
-                            cur_beg = cur_end;
-                            cur_end = static_cast<int>(static_cast<long long>(P.d_off[cur + 1]) - r_lo);
-                        }
-                    }
+                    for (int ch = 0; ch < BN / 32; ++ch)
+                        chunk_max_tmem(tmem + lane_base + buf * BN + ch * 32, r0 + ch * 32 - cur_beg, best, best_col,
+                                       hi_mask);
+                    if (cur_end == r0 + BN) close_doc();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bar.s_free[buf]);
@@ -282,44 +379,37 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int ch = 0; ch < BN / 32; ++ch) {
                     const int c0 = r0 + ch * 32;
                     if (c0 >= span) break;
-                    float v[32];
-                    tmem_ld32(tmem + lane_base + buf * BN + ch * 32, v);
+                    const uint32_t ta = tmem + lane_base + buf * BN + ch * 32;
                     const int hi_chunk = min(c0 + 32, span);
                     if (hi_chunk == c0 + 32 && cur_end >= c0 + 32) {
                         // the whole chunk lies inside the current document
-                        chunk_max<true>(v, 0, 32, c0 - cur_beg, best, best_col, hi_mask);
-                        if (cur_end == c0 + 32) {
-                            if (t_ok) {
-                                P.argmax[static_cast<long long>(cur) * P.ld_argmax + t] = best_col;
-                                P.mval[static_cast<long long>(cur) * P.rows_q + t] = best;
-                            }
-                            ++cur;
-                            best = -INFINITY;
-                            best_col = 0;
-                            if (cur < d1) {
-                                cur_beg = cur_end;
-                                cur_end = static_cast<int>(static_cast<long long>(P.d_off[cur + 1]) - r_lo);
-                            }
-                        }
+                        chunk_max_tmem(ta, c0 - cur_beg, best, best_col, hi_mask);
+                        if (cur_end == c0 + 32) close_doc();
                         continue;
                     }
+                    // The current document ends inside the chunk (warp-uniform: document boundaries are
+                    // shared by all rows).  With one boundary whose next document covers the rest of the
+                    // chunk, or at the end of the work item, the prefix and suffix maxima come from TMEM;
+                    // chunks holding more boundaries take the masked register tree per segment.
+                    const bool tail = hi_chunk < c0 + 32 && cur_end == hi_chunk;
+                    const bool split = hi_chunk == c0 + 32 && cur + 1 < d1 &&
+                                       static_cast<long long>(P.d_off[cur + 2]) - r_lo >= c0 + 32;
+                    if (tail || split) {
+                        chunk_keys_to_tmem(ta, hi_mask);
+                        float ma, mb;
+                        split_max(ta, cur_end - c0, split, ma, mb);
+                        update_best(ma, c0 - cur_beg, best, best_col);
+                        close_doc();
+                        if (split) update_best(mb, c0 - cur_beg, best, best_col);
+                        continue;
+                    }
+                    float v[32];
+                    tmem_ld32(ta, v);
                     int lo = c0;
-                    while (lo < hi_chunk) {   // warp-uniform: document boundaries are shared by all rows
+                    while (lo < hi_chunk) {
                         const int seg_hi = min(hi_chunk, cur_end);
-                        chunk_max<false>(v, lo - c0, seg_hi - c0, c0 - cur_beg, best, best_col, hi_mask);
-                        if (seg_hi == cur_end) {
-                            if (t_ok) {
-                                P.argmax[static_cast<long long>(cur) * P.ld_argmax + t] = best_col;
-                                P.mval[static_cast<long long>(cur) * P.rows_q + t] = best;
-                            }
-                            ++cur;
-                            best = -INFINITY;
-                            best_col = 0;
-                            if (cur < d1) {
-                                cur_beg = cur_end;
-                                cur_end = static_cast<int>(static_cast<long long>(P.d_off[cur + 1]) - r_lo);
-                            }
-                        }
+                        chunk_max(v, lo - c0, seg_hi - c0, c0 - cur_beg, best, best_col, hi_mask);
+                        if (seg_hi == cur_end) close_doc();
                         lo = seg_hi;
                     }
                 }
@@ -448,6 +538,10 @@ __global__ void qmap_kernel(const uint64_t *q_off, int nq, int32_t *qmap, const 
     for (uint64_t t = q_off[q]; t < q_off[q + 1]; ++t) qmap[t] = q;
 }
 
+// A row of zeros as wide as the widest token (256 bf16): the gather source of
+// a pair that adds nothing, so the gathers need neither branches nor masks.
+__device__ const uint4 kZeroRow[32] = {};
+
 // acc[i] += c * (the 8 bf16 of u), as four packed fp32 pair FMAs; u holds
 // features 2i (low half of word i) and 2i + 1 (high half).
 __device__ __forceinline__ void fma_bf16x8(float2 (&acc)[4], const uint4 u, float c) {
@@ -465,7 +559,10 @@ __device__ __forceinline__ void fma_bf16x8(float2 (&acc)[4], const uint4 u, floa
 // results by shuffles, so each thread then spends its instructions on the
 // 16-byte gathers and packed FMAs.  The loads that resolve the next step are
 // issued before this step's gathers, so a step waits on one round trip to L2,
-// not two.
+// not two.  Only the step's documents with c != 0 for some row of the warp are
+// gathered (a ballot over the group lanes; a loss that ignores pairs leaves
+// many c = 0), and a pair that adds nothing reads a row of zeros, so no load or
+// FMA is masked.
 constexpr int kDqRows = 32;
 constexpr int kDqUnroll = 8;
 template <int NBLK>   // 64-feature blocks of the width (1..4)
@@ -486,30 +583,84 @@ __global__ void __launch_bounds__(256, NBLK <= 2 ? 4 : 2) dq_kernel(MaxSimBwdLau
         for (int i = 0; i < 4; ++i) acc[k][i] = make_float2(0.f, 0.f);
     const float *dsrow = L.d_scores + static_cast<long long>(q) * L.ld_ds;
     const int32_t *amcol = L.argmax + tc;
-    // The raw loads that resolve document d ...
+    // The loads that resolve document d (its argmax entry and c) ...
     int a_n = 0;
-    uint64_t o_n = 0, e_n = 0;
     float c_n = 0.f;
     auto fetch = [&](int d) {
         if (d < L.nd) {
             a_n = __ldg(amcol + static_cast<long long>(d) * L.ld_argmax);
-            o_n = __ldg(L.d_off + d);
-            e_n = __ldg(L.d_off + d + 1);
             c_n = __ldg(dsrow + d);
         }
     };
-    // ... and their use: the gathered row (0 past the last document, for a rejected entry or for c = 0)
-    // and c.
+    // ... and their use, with the document's offsets (a small, cache-resident table): the gathered row
+    // (the zero row past the last document, for a rejected entry or for c = 0) and c.
+    const unsigned long long zero_row = reinterpret_cast<unsigned long long>(kZeroRow);
     auto finish = [&](int d, unsigned long long &src, float &c) {
-        src = 0;
+        src = zero_row;
         c = 0.f;
         if (d < L.nd) {
-            if (a_n < 0 || static_cast<uint64_t>(a_n) >= e_n - o_n) {
+            const uint64_t o = __ldg(L.d_off + d), e = __ldg(L.d_off + d + 1);
+            if (a_n < 0 || static_cast<uint64_t>(a_n) >= e - o) {
                 if (row_ok) report(L.status, CLI_MALFORMED);
             } else if (c_n != 0.0f) {   // a pair with c = 0 (one a loss ignores) gathers nothing
-                src = reinterpret_cast<unsigned long long>(L.d + (o_n + static_cast<uint64_t>(a_n)) * L.width);
+                src = reinterpret_cast<unsigned long long>(L.d + (o + static_cast<uint64_t>(a_n)) * L.width);
                 c = c_n * scale;
             }
+        }
+    };
+    // This thread's features of every 64-feature block (a block past the width reads the row's last 8
+    // features: they land in accumulators that are never stored).
+    int fo[NBLK];
+#pragma unroll
+    for (int k = 0; k < NBLK; ++k) fo[k] = min(k * 64 + sub * 8, L.width - 8);
+    // One step: this lane's group holds document d0 + u's row address and c in lane u of the group.
+    auto step = [&](unsigned long long src, float c) {
+        // The step's documents with c != 0 for some row of the warp, in order: the warp's rows usually
+        // belong to one query, so this is the step's active set, and a pair with c = 0 costs no gather.
+        const unsigned act = __ballot_sync(0xffffffffu, c != 0.0f);
+        unsigned mm = (act | (act >> 8) | (act >> 16) | (act >> 24)) & 0xFFu;
+        const int n_act = __popc(mm);
+        if (n_act == kDqUnroll) {
+            // Every document of the step: all eight rows' loads in flight together, then the FMAs (a row
+            // with c = 0 for a document reads the zero row).
+            uint4 x[kDqUnroll][NBLK];
+            float cu[kDqUnroll];
+#pragma unroll
+            for (int u = 0; u < kDqUnroll; ++u) {
+                const uint16_t *row = reinterpret_cast<const uint16_t *>(__shfl_sync(0xffffffffu, src, u, 8));
+                cu[u] = __shfl_sync(0xffffffffu, c, u, 8);
+#pragma unroll
+                for (int k = 0; k < NBLK; ++k) x[u][k] = __ldg(reinterpret_cast<const uint4 *>(row + fo[k]));
+            }
+#pragma unroll
+            for (int u = 0; u < kDqUnroll; ++u)
+#pragma unroll
+                for (int k = 0; k < NBLK; ++k) fma_bf16x8(acc[k], x[u][k], cu[u]);
+            return;
+        }
+        // The active documents four at a time, the same way (a slot past the last one reads the zero
+        // row with c = 0).
+        for (int u0 = 0; u0 < n_act; u0 += 4) {
+            uint4 x[4][NBLK];
+            float cu[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int p = mm != 0 ? __ffs(mm) - 1 : 0;
+                mm &= mm - 1;
+                unsigned long long sp = __shfl_sync(0xffffffffu, src, p, 8);
+                cu[u] = __shfl_sync(0xffffffffu, c, p, 8);
+                if (u0 + u >= n_act) {
+                    sp = zero_row;
+                    cu[u] = 0.f;
+                }
+                const uint16_t *row = reinterpret_cast<const uint16_t *>(sp);
+#pragma unroll
+                for (int k = 0; k < NBLK; ++k) x[u][k] = __ldg(reinterpret_cast<const uint4 *>(row + fo[k]));
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int k = 0; k < NBLK; ++k) fma_bf16x8(acc[k], x[u][k], cu[u]);
         }
     };
     unsigned long long src;
@@ -518,30 +669,7 @@ __global__ void __launch_bounds__(256, NBLK <= 2 ? 4 : 2) dq_kernel(MaxSimBwdLau
     finish(sub, src, c);
     for (int d0 = 0; d0 < L.nd; d0 += kDqUnroll) {
         fetch(d0 + kDqUnroll + sub);   // the next step's resolution, in flight during this step
-        unsigned long long su[kDqUnroll];
-        float cu[kDqUnroll];
-#pragma unroll
-        for (int u = 0; u < kDqUnroll; ++u) {
-            su[u] = __shfl_sync(0xffffffffu, src, u, 8);
-            cu[u] = __shfl_sync(0xffffffffu, c, u, 8);
-        }
-        // Unconditional loads (a missing row reads row 0 of the tape, a feature block past the
-        // width its last 8 features), masked afterwards: nothing branches between the gathers.
-        uint4 x[kDqUnroll][NBLK];
-#pragma unroll
-        for (int u = 0; u < kDqUnroll; ++u) {
-            const uint16_t *row = su[u] != 0 ? reinterpret_cast<const uint16_t *>(su[u]) : L.d;
-#pragma unroll
-            for (int k = 0; k < NBLK; ++k)
-                x[u][k] = __ldg(reinterpret_cast<const uint4 *>(row + min(k * 64 + sub * 8, L.width - 8)));
-        }
-#pragma unroll
-        for (int u = 0; u < kDqUnroll; ++u)
-#pragma unroll
-            for (int k = 0; k < NBLK; ++k) {
-                if (su[u] == 0 || k * 64 + sub * 8 >= L.width) x[u][k] = make_uint4(0, 0, 0, 0);
-                fma_bf16x8(acc[k], x[u][k], cu[u]);
-            }
+        step(src, c);
         finish(d0 + kDqUnroll + sub, src, c);
     }
     if (!row_ok) return;

@@ -40,6 +40,32 @@ def assert_rel(a, b, rtol, what):
     assert abs(a - b) <= rtol * max(abs(b), 1e-30), f"{what}: gpu {a!r} oracle {b!r}"
 
 
+def routed_argmax(m, gpu_arg, ora_arg, gap, rows=None, where=None):
+    """The argmax the reference gradient routes through, [documents, rows] like the tables given.
+
+    Where the oracle's top-2 gap exceeds ARGMAX_GAP the choice is unique and check_argmax has already
+    required the GPU to make it.  Elsewhere several rows are correct: the GPU's choice is kept after
+    checking that it lies inside its document and scores within ARGMAX_GAP of the oracle's row, so the
+    gradients are compared through the same valid routing.  `rows` maps the tables' columns to query-tape
+    rows (default: all rows in order); document d's rows start at m.d_offsets[d].  `where` (same shape)
+    limits the routing to the entries a gradient reads (named pairs)."""
+    use = np.array(ora_arg, dtype=np.int64, copy=True)
+    gpu_arg = np.asarray(gpu_arg)
+    rows = np.arange(use.shape[1]) if rows is None else np.asarray(rows)
+    open_choice = (np.asarray(gap) <= ARGMAX_GAP) & (gpu_arg != use)
+    todo = np.nonzero(open_choice if where is None else open_choice & where)
+    q, dm = (m.q, m.d) if todo[0].size else (None, None)
+    for d, c in zip(*todo):
+        r0, r1 = int(m.d_offsets[d]), int(m.d_offsets[d + 1])
+        jg, jo = int(gpu_arg[d, c]), int(use[d, c])
+        assert 0 <= jg < r1 - r0, f"argmax {jg} outside document {d}"
+        s_g = float(q[rows[c]] @ dm[r0 + jg])
+        s_o = float(q[rows[c]] @ dm[r0 + jo])
+        assert s_o - s_g <= ARGMAX_GAP, f"argmax {jg} of document {d} scores {s_g}, the maximum is {s_o}"
+        use[d, c] = jg
+    return use.astype(np.int32)
+
+
 def run_pooled(p, weights=None, ld=None, ld_de=None, repel=None):
     """Runs the pooled loss on the GPU for synth.PooledInputs p.  Returns numpy outputs and the status."""
     e_bits = p.e_bf16

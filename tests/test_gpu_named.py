@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from contrastive_late_interaction_gb300 import synth
-from tests.gpu_util import GRAD_RL2, bf16, check_argmax, check_scores, dev, i64, rel_l2
+from tests.gpu_util import GRAD_RL2, bf16, check_argmax, check_scores, dev, i64, rel_l2, routed_argmax
 
 pytestmark = pytest.mark.gpu
 
@@ -26,6 +26,12 @@ def named_lists(seed, nq, nd, k_lo, k_hi, own=False):
             docs.add(q % nd)
         lists.append(sorted(docs))
     return lists
+
+
+def row_mask(m, named):
+    """[documents, query rows] view of a [queries, documents] pair mask."""
+    q_of_row = np.repeat(np.arange(m.nq), np.diff(m.q_offsets.astype(np.int64)))
+    return named[q_of_row].T
 
 
 def run_named(m, lists):
@@ -73,7 +79,8 @@ def test_named_backward_matches_the_oracle():
                             torch.from_numpy(ds).to(dev()))
     torch.cuda.synchronize()
     assert int(g["device_status"].item()) == 0
-    _, arg, _ = oracle.maxsim_forward(m.q_offsets, m.q, m.d_offsets, m.d)
+    _, arg, gap = oracle.maxsim_forward(m.q_offsets, m.q, m.d_offsets, m.d)
+    arg = routed_argmax(m, r["argmax"].cpu().numpy(), arg, gap, where=row_mask(m, named))
     dq, dd = oracle.maxsim_backward(m.q_offsets, m.q, m.d_offsets, m.d, arg, ds.astype(np.float64))
     assert rel_l2(g["d_queries"].double().cpu().numpy(), dq) <= GRAD_RL2
     assert rel_l2(g["d_documents"].double().cpu().numpy(), dd) <= GRAD_RL2
@@ -117,7 +124,8 @@ def test_named_backward_ignores_pairs_not_named(mean):
     named = np.zeros((m.nq, m.nd), bool)
     for q, docs in enumerate(lists):
         named[q, docs] = True
-    _, arg, _ = oracle.maxsim_forward(m.q_offsets, m.q, m.d_offsets, m.d)
+    _, arg, gap = oracle.maxsim_forward(m.q_offsets, m.q, m.d_offsets, m.d)
+    arg = routed_argmax(m, f["argmax"].cpu().numpy(), arg, gap, where=row_mask(m, named))
     ds = np.where(named, m.d_scores, 0.0)
     dq, dd = oracle.maxsim_backward(m.q_offsets, m.q, m.d_offsets, m.d, arg, ds, mean)
     assert rel_l2(g["d_queries"].double().cpu().numpy(), dq) <= GRAD_RL2

@@ -17,7 +17,7 @@ pytestmark = [pytest.mark.gpu,
 if torch.cuda.is_available():
     import contrastive_late_interaction_gb300 as cli
     from tests.gpu_util import (GRAD_RL2, LOSS_RTOL, assert_rel, bf16, check_argmax, check_scores, i64, rel_l2,
-                                run_maxsim, run_pooled, scalar, dev)
+                                routed_argmax, run_maxsim, run_pooled, scalar, dev)
 
 
 # ---------------------------------------------------------------------------
@@ -140,6 +140,7 @@ def compare_maxsim_full(m, mean=False):
     check_scores(g["scores"], s)
     decided = check_argmax(g["argmax"], arg, gap)
     assert decided > 0.9 * arg.size
+    arg = routed_argmax(m, g["argmax"], arg, gap)
     dq, dd = oracle.maxsim_backward(m.q_offsets, m.q, m.d_offsets, m.d, arg, m.d_scores, mean)
     assert rel_l2(g["dq"], dq) <= GRAD_RL2
     assert rel_l2(g["dd"], dd) <= GRAD_RL2
@@ -197,13 +198,22 @@ def test_maxsim_config3_sampled():
     for k in range(len(pq)):
         t0, t1 = int(m.q_offsets[pq[k]]), int(m.q_offsets[pq[k] + 1])
         check_argmax(g["argmax"][pd[k], t0:t1], pa[k], pg[k])
-    for qi in (0, 311):
+    for qi in (0, 311):   # dQ of one query: the oracle's backward over (query qi, every document)
         t0, t1 = int(m.q_offsets[qi]), int(m.q_offsets[qi + 1])
-        ref = oracle.maxsim_grad_query(m.q_offsets, m.q, m.d_offsets, m.d, qi, m.d_scores[qi])
+        alld = np.arange(m.nd)
+        _, pa, pg = oracle.maxsim_pairs(m.q_offsets, m.q, m.d_offsets, m.d, np.full(m.nd, qi), alld)
+        arg = routed_argmax(m, g["argmax"][:, t0:t1], np.stack(pa), np.stack(pg), rows=np.arange(t0, t1))
+        ref, _ = oracle.maxsim_backward(np.array([0, t1 - t0], np.uint64), m.q[t0:t1], m.d_offsets, m.d, arg,
+                                        m.d_scores[qi:qi + 1])
         assert rel_l2(g["dq"][t0:t1], ref) <= GRAD_RL2
-    for di in (0, 499):
+    for di in (0, 499):   # dD of one document: the oracle's backward over (every query, document di)
         r0, r1 = int(m.d_offsets[di]), int(m.d_offsets[di + 1])
-        ref = oracle.maxsim_grad_doc(m.q_offsets, m.q, m.d_offsets, m.d, di, m.d_scores[:, di])
+        allq = np.arange(m.nq)
+        _, pa, pg = oracle.maxsim_pairs(m.q_offsets, m.q, m.d_offsets, m.d, allq, np.full(m.nq, di))
+        sub = synth.MaxSimInputs(m.width, m.q_offsets, m.q_bf16, np.array([0, r1 - r0], np.uint64),
+                                 m.d_bf16[r0:r1], m.d_scores[:, di:di + 1])
+        arg = routed_argmax(sub, g["argmax"][di:di + 1], np.concatenate(pa)[None, :], np.concatenate(pg)[None, :])
+        _, ref = oracle.maxsim_backward(m.q_offsets, m.q, sub.d_offsets, sub.d, arg, sub.d_scores)
         assert rel_l2(g["dd"][r0:r1], ref) <= GRAD_RL2
 
 
