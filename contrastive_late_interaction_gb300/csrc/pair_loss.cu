@@ -26,14 +26,19 @@
 //      w (sp - [attract] z).  H_xy = (t/N) G_xy goes to shared memory as bf16;
 //      partial sums of the loss, G*s (for dt) and G (for db) go to a fixed
 //      slot per warp.
-//   3. Gradient pass.  Per 64 columns of D, tcgen05 accumulates
-//          dE_Ix += sum_y H_xy E_Jy,   dE_Jy += sum_x H_xy^T E_Ix
-//      in four TMEM accumulators (two on a diagonal block, where the rows and
-//      columns coincide), reading H and the E boxes in both K-major and
-//      MN-major form from the same bytes; the epilogue warps add each chunk
-//      into dE (fp32) while the next chunk's MMAs run, each vector reduction
-//      covering 128 contiguous bytes of four rows after a transpose through
-//      shared memory (the L2 reductions cost per request, not per byte).
+//   3. Gradient passes.  Per 128 columns of D, tcgen05 accumulates
+//          dE_Ix += sum_y H_xy E_Jy    (pass 0, the row side)
+//          dE_Jy += sum_x H_xy^T E_Ix  (pass 1, the column side; none on a
+//                                        diagonal block, where pass 0 takes
+//                                        the one mirrored product)
+//      in two TMEM accumulators of 128 columns, double-buffered, reading H
+//      and the E boxes in both K-major and MN-major form from the same bytes
+//      (N = 128 products: per product the H operand is read once for 128
+//      features, not 64, which is what the shared-memory bandwidth of this
+//      pass pays for); the epilogue warps add each chunk into dE (fp32) while
+//      the next chunk's MMAs run, each vector reduction covering 128
+//      contiguous bytes of four rows after a transpose through shared memory
+//      (the L2 reductions cost per request, not per byte).
 // Each accumulator sums the contributions of two tiles before it leaves the
 // SM, so per FLOP half as many fp32 partials reach L2 as with single tile
 // pairs: L2 reductions of dE are what bound this kernel.  Neither S nor H ever
@@ -181,6 +186,22 @@ __device__ __forceinline__ bool box_on(const Block &b, int pos) {
 }
 __device__ __forceinline__ int col_pos(const Block &b, int y) { return b.diag ? y : 2 + y; }
 __device__ __forceinline__ int box_tile(const Block &b, int pos) { return pos < 2 ? b.I0 + pos : b.J0 + pos - 2; }
+
+// Gradient schedule of a block.  Pass 0 is the row side (dE of I0, I1) and,
+// off the diagonal, pass 1 the column side (dE of J0, J1); each runs over
+// chunks of 128 features (two 64-feature boxes per tile).  In pass 0 ring half
+// h holds the two feature boxes of tile J_h (of I_h on a diagonal block, whose
+// column tiles are its rows); in pass 1 those of I_h.
+__device__ __forceinline__ int grad_passes(const Block &b) { return b.diag ? 1 : 2; }
+__device__ __forceinline__ int grad_half_tile(const Block &b, int pass, int h) {   // -1: absent
+    if (pass == 0 && !b.diag) return (h == 0 || b.j1) ? b.J0 + h : -1;
+    return (h == 0 || b.i1) ? b.I0 + h : -1;
+}
+// The tile row whose dE accumulator a (0, 1) collects in pass `pass` (-1: none).
+__device__ __forceinline__ int grad_acc_tile(const Block &b, int pass, int a) {
+    if (pass == 0) return (a == 0 || b.i1) ? b.I0 + a : -1;
+    return (a == 0 || b.j1) ? b.J0 + a : -1;
+}
 
 __device__ __forceinline__ float fast_ex2(float x) {
     float y;
@@ -342,6 +363,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ph ^= 1u << bit;
                 return true;
             };
+            // Ring half h: the two 64-feature boxes of `tile` from feature k0 (none when the tile is absent;
+            // a box past the width reads zeros).
+            const int nc = (P.nk + 1) / 2;
+            auto load_grad_half = [&](int h, int tile, int k0) -> bool {
+                const int bit = 3 + h;
+                if (!mbar_wait(&sm.ring_empty[h], ((ph >> bit) & 1) ^ 1, abort_flag, P.status, kSleepProducer)) return false;
+                mbar_arrive_expect_tx(&sm.ring_full[h], tile >= 0 ? 2 * BOX_BYTES : 0u);
+                if (tile >= 0) {
+                    tma_load_2d(sm.ring[2 * h], &tmap_e, &sm.ring_full[h], k0, tile * BM);
+                    tma_load_2d(sm.ring[2 * h + 1], &tmap_e, &sm.ring_full[h], k0 + BK, tile * BM);
+                }
+                ph ^= 1u << bit;
+                return true;
+            };
             for (long long p = blockIdx.x; p < P.blocks && ok; p += gridDim.x, ++kblk) {
                 const Block bk = decode_block(p, P);
                 int nbox = 0;
@@ -366,9 +401,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_2d(box_ptr(s, pos), &tmap_e, &sm.full[s], kc * BK, box_tile(bk, pos) * BM);
                     ph ^= 1u << s;
                 }
-                // Gradient pass: the J half first, which the row-side products read first, so that
-                // each half loads while the other half's products run.
-                for (int dc = 0; dc < P.nk && ok; ++dc) ok = load_half(bk, 1, dc * BK) && load_half(bk, 0, dc * BK);
+                // Gradient passes: per 128-feature chunk ring half 0, then half 1, so that each half loads
+                // while the other half's products run.
+                for (int pass = 0; pass < grad_passes(bk) && ok; ++pass)
+                    for (int c = 0; c < nc && ok; ++c)
+                        for (int h = 0; h < 2 && ok; ++h) ok = load_grad_half(h, grad_half_tile(bk, pass, h), c * 2 * BK);
             }
             // Let in-flight loads land before the CTA can exit.
             for (int s = 1; s < kStages; ++s) mbar_wait(&sm.empty[s], ((ph >> s) & 1) ^ 1, abort_flag, P.status);
@@ -378,8 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16(128, 256, 0, 0);
-            const uint32_t idesc_row = idesc_bf16(128, 64, 0, 1);   // A = H (K-major), B = E_J (MN-major)
-            const uint32_t idesc_col = idesc_bf16(128, 64, 1, 1);   // A = H^T (MN-major), B = E_I (MN-major)
+            const uint32_t idesc_row = idesc_bf16(128, 128, 0, 1);   // A = H (K-major), B = E (MN-major)
+            const uint32_t idesc_col = idesc_bf16(128, 128, 1, 1);   // A = H^T (MN-major), B = E (MN-major)
             uint32_t ph = 0;   // bit s (1, 2): parity of H-region stage s's next use; bit 3 + h: of ring half h
             uint32_t kblk = 0, chunk = 0;
             bool ok = true;
@@ -429,59 +466,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 mma_commit(&sm.s_full);
-                // Gradient pass, 64 columns of D at a time, into TMEM buffer (chunk & 1).
+                // Gradient passes, 128 features at a time, into TMEM buffer (chunk & 1): accumulator a of
+                // the pass at columns a * 128.  Products are M = 128, N = 128, K = 16; the B operand is a
+                // tile's two feature boxes of ring half h, adjacent in shared memory, viewed as
+                // [N = 128 features] x [K = rows] (MN-major, the boxes BOX_BYTES apart).
                 if (!mbar_wait(&sm.h_ready, kblk & 1, abort_flag, P.status, kSleepIssuer)) break;
                 tc_fence_after();
-                for (int dc = 0; dc < P.nk; ++dc, ++chunk) {
-                    const uint32_t buf = chunk & 1;
-                    if (!mbar_wait(&sm.de_free[buf], ((chunk >> 1) & 1) ^ 1, abort_flag, P.status, kSleepIssuer)) { ok = false; break; }
-                    const uint32_t acc0 = tmem + buf * 256;
-                    uint32_t started = 0;   // bit a: accumulator a holds this chunk's first product
-                    // Row side: acc[x] += H_xy E_Jy.  A: H rows i, K = j (16 per step) inside 64-wide
-                    // K blocks; B: the E_Jy box viewed as [N = 64 features] x [K = j].
-                    auto row_side = [&]() {
-#pragma unroll
-                        for (int x = 0; x < 2; ++x)
-#pragma unroll
-                            for (int y = 0; y < 2; ++y) {
-                                if (!slot_on(bk, x, y)) continue;
-                                const uint32_t h = smem_u32(sm.hreg[2 * (2 * x + y)]);
-                                const uint32_t ej = smem_u32(sm.ring[col_pos(bk, y)]);
-#pragma unroll
-                                for (int kk = 0; kk < BM / 16; ++kk)
-                                    mma_bf16(acc0 + x * 64, sdesc_sw128(h + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024),
-                                             sdesc_sw128(ej + kk * 2048, 1024, 1024), idesc_row,
-                                             ((started >> x) & 1) || kk != 0);
-                                started |= 1u << x;
-                            }
-                    };
-                    if (!wait_half(1)) { ok = false; break; }
-                    tc_fence_after();
-                    if (!bk.diag) row_side();
-                    free_half(1);
-                    if (!wait_half(0)) { ok = false; break; }
-                    tc_fence_after();
-                    if (bk.diag) row_side();   // on a diagonal block the column tiles are I0, I1
-                    // Column side: acc[col] += H_xy^T E_Ix.  A: H viewed as [M = j] x [K = i], j
-                    // contiguous within a 64-wide block (blocks BOX_BYTES apart), 8 rows of i per 1024
-                    // bytes.  A diagonal tile's H is symmetric: its row side is all of it.
-#pragma unroll
-                    for (int x = 0; x < 2; ++x)
-#pragma unroll
-                        for (int y = 0; y < 2; ++y) {
-                            if (!slot_on(bk, x, y) || (bk.diag && x == y)) continue;
+                const int nc = (P.nk + 1) / 2;
+                for (int pass = 0; pass < grad_passes(bk) && ok; ++pass)
+                    for (int c = 0; c < nc; ++c, ++chunk) {
+                        const uint32_t buf = chunk & 1;
+                        if (!mbar_wait(&sm.de_free[buf], ((chunk >> 1) & 1) ^ 1, abort_flag, P.status, kSleepIssuer)) { ok = false; break; }
+                        const uint32_t acc0 = tmem + buf * 256;
+                        uint32_t started = 0;   // bit a: accumulator a holds this chunk's first product
+                        // acc[a] += H_xy E (A: H rows i, K = j, K-major) or H_xy^T E (A: H viewed as [M = j] x
+                        // [K = i], MN-major, j contiguous within a 64-wide block, blocks BOX_BYTES apart).
+                        auto product = [&](int a, int x, int y, bool transposed, uint32_t eb) {
                             const uint32_t h = smem_u32(sm.hreg[2 * (2 * x + y)]);
-                            const int ca = col_pos(bk, y);
-                            const uint32_t ei = smem_u32(sm.ring[x]);
 #pragma unroll
-                            for (int kk = 0; kk < BM / 16; ++kk)
-                                mma_bf16(acc0 + ca * 64, sdesc_sw128(h + kk * 2048, BOX_BYTES, 1024),
-                                         sdesc_sw128(ei + kk * 2048, 1024, 1024), idesc_col, ((started >> ca) & 1) || kk != 0);
-                            started |= 1u << ca;
+                            for (int kk = 0; kk < BM / 16; ++kk) {
+                                const uint64_t ad = transposed ? sdesc_sw128(h + kk * 2048, BOX_BYTES, 1024)
+                                                               : sdesc_sw128(h + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
+                                mma_bf16(acc0 + a * 128, ad, sdesc_sw128(eb + kk * 2048, BOX_BYTES, 1024),
+                                         transposed ? idesc_col : idesc_row, ((started >> a) & 1) || kk != 0);
+                            }
+                            started |= 1u << a;
+                        };
+                        for (int h = 0; h < 2; ++h) {
+                            if (!wait_half(h)) { ok = false; break; }
+                            tc_fence_after();
+                            if (grad_half_tile(bk, pass, h) >= 0) {
+                                const uint32_t eb = smem_u32(sm.ring[2 * h]);
+                                if (bk.diag) {
+                                    // E of I_h: row side of the slots (x, h), and the column side of (0, 1)
+                                    // into I1 (a diagonal tile's H is symmetric: its row side is all of it).
+                                    for (int x = 0; x < 2; ++x)
+                                        if (slot_on(bk, x, h)) product(x, x, h, false, eb);
+                                    if (h == 0 && slot_on(bk, 0, 1)) product(1, 0, 1, true, eb);
+                                } else if (pass == 0) {   // E of J_h: dE_Ix += H_xh E_Jh
+                                    for (int x = 0; x < 2; ++x)
+                                        if (slot_on(bk, x, h)) product(x, x, h, false, eb);
+                                } else {                  // E of I_h: dE_Jy += H_hy^T E_Ih
+                                    for (int y = 0; y < 2; ++y)
+                                        if (slot_on(bk, h, y)) product(y, h, y, true, eb);
+                                }
+                            }
+                            free_half(h);
                         }
-                    free_half(0);
-                    mma_commit(&sm.de_full[buf]);
-                }
+                        if (!ok) break;
+                        mma_commit(&sm.de_full[buf]);
+                    }
                 if (!ok) break;
                 mma_commit(&sm.h_free);
             }
@@ -628,44 +662,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 slot[2] = g_sum;
                 slot[3] = 0.f;
             }
-            // Drain the gradient chunks into dE: this warp takes accumulators x and 2 + x.
+            // Drain the gradient chunks into dE: this warp takes accumulator x of each pass.
             bool ok = true;
-            for (int dc = 0; dc < P.nk; ++dc, ++chunk) {
-                const uint32_t buf = chunk & 1;
-                if (!mbar_wait(&sm.de_full[buf], (chunk >> 1) & 1, abort_flag, P.status, kSleepEpilogue)) { ok = false; break; }
-                tc_fence_after();
+            const int nc = (P.nk + 1) / 2;
+            for (int pass = 0; pass < grad_passes(bk) && ok; ++pass)
+                for (int c = 0; c < nc; ++c, ++chunk) {
+                    const uint32_t buf = chunk & 1;
+                    if (!mbar_wait(&sm.de_full[buf], (chunk >> 1) & 1, abort_flag, P.status, kSleepEpilogue)) { ok = false; break; }
+                    tc_fence_after();
+                    const int tile = grad_acc_tile(bk, pass, x);   // warp-uniform; -1: an absent tile row
+                    if (tile >= 0) {
+                        const int row0 = tile * BM + quad * 32;     // first row of this warp's 32
 #pragma unroll 1
-                for (int a = x; a < 4; a += 2) {
-                    if (!box_on(bk, a)) continue;   // warp-uniform: the accumulator of an absent tile row
-                    const int row0 = box_tile(bk, a) * BM + quad * 32;   // first row of this warp's 32
-#pragma unroll 1
-                    for (int half = 0; half < 2; ++half) {
-                        float v[32];
-                        tmem_ld32(tmem + lane_base + buf * 256 + a * 64 + half * 32, v);
-                        // lane = row: its 32 values as 8 x 16 B, chunk index swizzled by row
+                        for (int piece = 0; piece < 4; ++piece) {
+                            const int c0 = c * 128 + piece * 32;
+                            if (c0 >= P.width) break;
+                            float v[32];
+                            tmem_ld32(tmem + lane_base + buf * 256 + x * 128 + piece * 32, v);
+                            // lane = row: its 32 values as 8 x 16 B, chunk index swizzled by row
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            st_shared_v4(stage_s + (lane * 32 + ((k ^ (lane & 7)) * 4)) * 4, __float_as_uint(v[k * 4]),
-                                         __float_as_uint(v[k * 4 + 1]), __float_as_uint(v[k * 4 + 2]),
-                                         __float_as_uint(v[k * 4 + 3]));
-                        __syncwarp();
-                        // read back: instruction m covers rows 4m .. 4m+3, 8 lanes x 16 B = 128 B per row
-                        const int col = dc * BK + half * 32 + (lane & 7) * 4;
+                            for (int k = 0; k < 8; ++k)
+                                st_shared_v4(stage_s + (lane * 32 + ((k ^ (lane & 7)) * 4)) * 4, __float_as_uint(v[k * 4]),
+                                             __float_as_uint(v[k * 4 + 1]), __float_as_uint(v[k * 4 + 2]),
+                                             __float_as_uint(v[k * 4 + 3]));
+                            __syncwarp();
+                            // read back: instruction m covers rows 4m .. 4m+3, 8 lanes x 16 B = 128 B per row
+                            const int col = c0 + (lane & 7) * 4;
 #pragma unroll
-                        for (int m = 0; m < 8; ++m) {
-                            const int r = m * 4 + (lane >> 3);
-                            const float4 xv = *reinterpret_cast<const float4 *>(&sm.stage_t[ew][r * 32 + (((lane & 7) ^ (r & 7)) * 4)]);
-                            const int grow = row0 + r;
-                            if (grow < P.n && col < P.width)
-                                red_add_v4(P.d_e + static_cast<long long>(grow) * P.ld_de + col, xv.x, xv.y, xv.z, xv.w);
+                            for (int m = 0; m < 8; ++m) {
+                                const int r = m * 4 + (lane >> 3);
+                                const float4 xv = *reinterpret_cast<const float4 *>(&sm.stage_t[ew][r * 32 + (((lane & 7) ^ (r & 7)) * 4)]);
+                                const int grow = row0 + r;
+                                if (grow < P.n && col < P.width)
+                                    red_add_v4(P.d_e + static_cast<long long>(grow) * P.ld_de + col, xv.x, xv.y, xv.z, xv.w);
+                            }
+                            __syncwarp();
                         }
-                        __syncwarp();
                     }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.de_free[buf]);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.de_free[buf]);
-            }
             if (!ok) break;
         }
     }
