@@ -630,11 +630,10 @@ cli_status_t maxsim_scores_named(const cli_maxsim_named_t *a) {
 
 size_t maxsim_backward_workspace_bytes(size_t query_count, size_t document_count, size_t query_rows,
                                        size_t document_rows, size_t width) {
-    (void)query_count;
-    (void)document_count;
     (void)document_rows;
     (void)width;
-    return align256(query_rows * sizeof(int32_t));
+    // the row -> query map, then one activity flag per query and per document
+    return align256(query_rows * sizeof(int32_t)) + align256(query_count) + align256(document_count);
 }
 
 }  // extern "C"
@@ -696,6 +695,11 @@ cli_status_t maxsim_backward_call(const cli_maxsim_backward_t *a, const cli_edge
     L.dq = a->d_queries;
     L.dd = a->d_documents;
     L.qmap = static_cast<int32_t *>(a->workspace);
+    if (!pairs) {
+        uint8_t *w = static_cast<uint8_t *>(a->workspace) + align256(rq * sizeof(int32_t));
+        L.q_active = w;
+        L.d_active = w + align256(nq);
+    }
     L.status = a->device_status;
     L.sm_count = sms;
     if (pairs) {

@@ -151,6 +151,10 @@ struct MaxSimBwdLaunch {
     int32_t *qmap;            // workspace [rows_q]
     int32_t *status;
     int sm_count;
+    // Workspace flags (null: every query and document active): whether some c(q, d) of query q, of
+    // document d, is nonzero.  The backward skips the rows of inactive ones.
+    uint8_t *q_active = nullptr;   // [nq]
+    uint8_t *d_active = nullptr;   // [nd]
 };
 cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream);
 // The backward over named pairs only (dQ and dD zeroed by the caller).

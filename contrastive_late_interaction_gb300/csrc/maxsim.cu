@@ -531,6 +531,41 @@ __global__ void query_sum_kernel(const float *mval, const uint64_t *q_off, int n
 // backward
 // ----------------------------------------------------------------------------
 
+// q_active[q] = 1 when some c(q, d) is nonzero, d_active[d] = 1 when some
+// c(q, d) is (one block per query; both zeroed beforehand, every writer
+// writes 1).
+__global__ void active_kernel(const float *d_scores, long long ld_ds, int nd, uint8_t *q_active, uint8_t *d_active,
+                              const int32_t *status) {
+    if (read_status(status) != 0) return;
+    const int q = blockIdx.x;
+    const float *row = d_scores + static_cast<long long>(q) * ld_ds;
+    int any = 0;
+    for (int d = threadIdx.x; d < nd; d += blockDim.x)
+        if (row[d] != 0.0f) {
+            any = 1;
+            d_active[d] = 1;
+        }
+    if (__syncthreads_or(any) && threadIdx.x == 0) q_active[q] = 1;
+}
+
+// The dD rows of a document no query scores are zero; its argmax entries are
+// still checked (active documents check theirs in dd_sort_kernel).
+__global__ void dd_zero_kernel(MaxSimBwdLaunch L) {
+    if (read_status(L.status) != 0) return;
+    const int d = blockIdx.x;
+    if (L.d_active[d]) return;
+    const uint64_t o0 = L.d_off[d];
+    const int dl = static_cast<int>(L.d_off[d + 1] - o0);
+    const int32_t *am = L.argmax + static_cast<long long>(d) * L.ld_argmax;
+    for (int k = threadIdx.x; k < L.rows_q; k += blockDim.x) {
+        const int a = __ldg(am + k);
+        if (a < 0 || a >= dl) report(L.status, CLI_MALFORMED);
+    }
+    float4 *dst = reinterpret_cast<float4 *>(L.dd + static_cast<long long>(o0) * L.width);
+    const long long n4 = static_cast<long long>(dl) * L.width / 4;
+    for (long long i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 __global__ void qmap_kernel(const uint64_t *q_off, int nq, int32_t *qmap, const int32_t *status) {
     if (read_status(status) != 0) return;
     const int q = blockIdx.x * blockDim.x + threadIdx.x;
@@ -583,6 +618,8 @@ __global__ void __launch_bounds__(256, NBLK <= 2 ? 4 : 2) dq_kernel(MaxSimBwdLau
         for (int i = 0; i < 4; ++i) acc[k][i] = make_float2(0.f, 0.f);
     const float *dsrow = L.d_scores + static_cast<long long>(q) * L.ld_ds;
     const int32_t *amcol = L.argmax + tc;
+    // A warp whose rows all belong to queries no document scores with c != 0 stores zeros.
+    const bool warp_idle = __all_sync(0xffffffffu, L.q_active != nullptr && L.q_active[q] == 0);
     // The loads that resolve document d (its argmax entry and c) ...
     int a_n = 0;
     float c_n = 0.f;
@@ -667,7 +704,7 @@ __global__ void __launch_bounds__(256, NBLK <= 2 ? 4 : 2) dq_kernel(MaxSimBwdLau
     float c;
     fetch(sub);
     finish(sub, src, c);
-    for (int d0 = 0; d0 < L.nd; d0 += kDqUnroll) {
+    for (int d0 = 0; d0 < (warp_idle ? 0 : L.nd); d0 += kDqUnroll) {
         fetch(d0 + kDqUnroll + sub);   // the next step's resolution, in flight during this step
         step(src, c);
         finish(d0 + kDqUnroll + sub, src, c);
@@ -770,6 +807,7 @@ __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch 
     __shared__ uint32_t warp_sums[kDsThreads / 32];
     if (read_status(L.status) != 0) return;
     const int d = blockIdx.x;
+    if (L.d_active && !L.d_active[d]) return;   // dd_zero_kernel writes its rows
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint64_t o0 = L.d_off[d];
     const int dl = static_cast<int>(L.d_off[d + 1] - o0);
@@ -1021,6 +1059,15 @@ cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream
     cudaError_t err;
     qmap_kernel<<<(L.nq + 255) / 256, 256, 0, stream>>>(L.q_off, L.nq, L.qmap, L.status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (L.q_active) {
+        if ((err = cudaMemsetAsync(L.q_active, 0, L.nq, stream)) != cudaSuccess ||
+            (err = cudaMemsetAsync(L.d_active, 0, L.nd, stream)) != cudaSuccess)
+            return err;
+        active_kernel<<<L.nq, 256, 0, stream>>>(L.d_scores, L.ld_ds, L.nd, L.q_active, L.d_active, L.status);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        dd_zero_kernel<<<L.nd, 256, 0, stream>>>(L);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
     const unsigned dq_grid = (L.rows_q + kDqRows - 1) / kDqRows;
     switch ((L.width + 63) / 64) {
         case 1: dq_kernel<1><<<dq_grid, 256, 0, stream>>>(L); break;

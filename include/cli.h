@@ -358,6 +358,11 @@ size_t maxsim_named_workspace_bytes(size_t query_count, size_t document_count, s
  *   d_scores      device fp32 [queries.count x ld_d_scores]
  *   d_queries     device fp32 [queries.rows x width] (written)
  *   d_documents   device fp32 [documents.rows x width] (written)
+ *   workspace     device, >= maxsim_backward_workspace_bytes(...), 256-byte
+ *                 aligned: the row -> query map and one flag per query and
+ *                 per document (whether some c is nonzero: the rows of a
+ *                 query or document with c = 0 throughout are written as
+ *                 zeros without gathering); contents on entry are ignored
  */
 typedef struct {
     cli_tape_t queries, documents;
