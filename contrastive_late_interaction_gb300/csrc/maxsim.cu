@@ -557,10 +557,13 @@ __global__ void dd_zero_kernel(MaxSimBwdLaunch L) {
     const uint64_t o0 = L.d_off[d];
     const int dl = static_cast<int>(L.d_off[d + 1] - o0);
     const int32_t *am = L.argmax + static_cast<long long>(d) * L.ld_argmax;
-    for (int k = threadIdx.x; k < L.rows_q; k += blockDim.x) {
+    bool bad = false;
+#pragma unroll 8
+    for (int k = threadIdx.x; k < L.rows_q; k += blockDim.x) {   // independent loads, one report at the end
         const int a = __ldg(am + k);
-        if (a < 0 || a >= dl) report(L.status, CLI_MALFORMED);
+        bad |= a < 0 || a >= dl;
     }
+    if (bad) report(L.status, CLI_MALFORMED);
     float4 *dst = reinterpret_cast<float4 *>(L.dd + static_cast<long long>(o0) * L.width);
     const long long n4 = static_cast<long long>(dl) * L.width / 4;
     for (long long i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1065,7 +1068,7 @@ cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream
             return err;
         active_kernel<<<L.nq, 256, 0, stream>>>(L.d_scores, L.ld_ds, L.nd, L.q_active, L.d_active, L.status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
-        dd_zero_kernel<<<L.nd, 256, 0, stream>>>(L);
+        dd_zero_kernel<<<L.nd, 512, 0, stream>>>(L);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     const unsigned dq_grid = (L.rows_q + kDqRows - 1) / kDqRows;
