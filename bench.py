@@ -39,7 +39,7 @@ L2_FLUSH_BYTES = 256 << 20
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["joint", "pooled2", "maxsim3", "pooled4", "matryoshka5", "groups5", "named5"], default="joint")
@@ -358,33 +358,69 @@ class Step:
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
+    """nvidia-smi sampling every 50 ms on a reader thread that stamps each line on arrival.  Entering
+    waits (up to 5 s) for the first line, so the sampler is running before the timed region starts;
+    mark() brackets the region, and summary() keeps the lines that arrived inside it (plus one
+    interval), or the nearest line after it if none did."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_S = 0.05
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.stamped = []
         self.lines = []
+        self.t0 = self.t1 = None
+        self.thread = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            if ln.strip():
+                self.stamped.append((time.monotonic(), ln))
 
     def __enter__(self):
+        import threading
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(int(self.INTERVAL_S * 1000))],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        deadline = time.monotonic() + 5.0
+        while not self.stamped and time.monotonic() < deadline and self.proc.poll() is None:
+            time.sleep(0.01)
         return self
+
+    def mark(self, start: bool):
+        if start:
+            self.t0 = time.monotonic()
+        else:
+            self.t1 = time.monotonic()
+            time.sleep(2 * self.INTERVAL_S)   # let the last in-region sample arrive
 
     def __exit__(self, *exc):
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+                self.proc.wait()
+            if self.thread is not None:
+                self.thread.join(timeout=5)
+        lines = list(self.stamped)
+        if self.t0 is not None and self.t1 is not None:
+            inside = [ln for t, ln in lines if self.t0 <= t <= self.t1 + self.INTERVAL_S]
+            if not inside:
+                after = [ln for t, ln in lines if t >= self.t0]
+                inside = after[:1]
+            lines = [(0.0, ln) for ln in inside]
+        self.lines = [ln for _, ln in lines]
 
     def summary(self):
         sm, smax, power, reasons = [], [], [], set()
@@ -608,6 +644,7 @@ def main():
         pg.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        clocks.mark(True)
         wall0 = time.perf_counter()
         for k in range(args.steps):
             with torch.cuda.stream(stream):
@@ -617,6 +654,7 @@ def main():
                 st_ev[k][1].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
+        clocks.mark(False)
     if pg is not None:
         pg.barrier()
     step_ms = [s.elapsed_time(e) for s, e in st_ev]
