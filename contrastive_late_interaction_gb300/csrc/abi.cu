@@ -632,8 +632,10 @@ size_t maxsim_backward_workspace_bytes(size_t query_count, size_t document_count
                                        size_t document_rows, size_t width) {
     (void)document_rows;
     (void)width;
-    // the row -> query map, then one activity flag per query and per document
-    return align256(query_rows * sizeof(int32_t)) + align256(query_count) + align256(document_count);
+    // the row -> query map, one activity flag per query and per document, the list of active documents
+    // and its length
+    return align256(query_rows * sizeof(int32_t)) + align256(query_count) + align256(document_count) +
+           align256(document_count * sizeof(uint32_t)) + 256;
 }
 
 }  // extern "C"
@@ -699,6 +701,8 @@ cli_status_t maxsim_backward_call(const cli_maxsim_backward_t *a, const cli_edge
         uint8_t *w = static_cast<uint8_t *>(a->workspace) + align256(rq * sizeof(int32_t));
         L.q_active = w;
         L.d_active = w + align256(nq);
+        L.d_list = reinterpret_cast<uint32_t *>(L.d_active + align256(nd));
+        L.d_count = L.d_list + align256(nd * sizeof(uint32_t)) / sizeof(uint32_t);
     }
     L.status = a->device_status;
     L.sm_count = sms;

@@ -155,6 +155,8 @@ struct MaxSimBwdLaunch {
     // document d, is nonzero.  The backward skips the rows of inactive ones.
     uint8_t *q_active = nullptr;   // [nq]
     uint8_t *d_active = nullptr;   // [nd]
+    uint32_t *d_list = nullptr;    // [nd]: the active documents in order (dQ walks these only)
+    uint32_t *d_count = nullptr;   // [1]: their number
 };
 cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream);
 // The backward over named pairs only (dQ and dD zeroed by the caller).

@@ -451,9 +451,9 @@ __global__ void mark_items_kernel(const uint64_t *q_off, const uint64_t *pair_of
 // The flagged items in index order (chunk-major) and their count: one block,
 // each thread compacting a contiguous segment after a scan of the counts.
 constexpr int kCompactThreads = 1024;
-__global__ void __launch_bounds__(kCompactThreads) compact_items_kernel(const uint32_t *flags, long long n,
-                                                                        uint32_t *list, uint32_t *count,
-                                                                        const int32_t *status) {
+template <typename F>
+__global__ void __launch_bounds__(kCompactThreads) compact_items_kernel(const F *flags, long long n, uint32_t *list,
+                                                                        uint32_t *count, const int32_t *status) {
     __shared__ uint32_t part[kCompactThreads];
     if (read_status(status) != 0) return;
     const long long per = (n + kCompactThreads - 1) / kCompactThreads;
@@ -623,22 +623,28 @@ __global__ void __launch_bounds__(256, NBLK <= 2 ? 4 : 2) dq_kernel(MaxSimBwdLau
     const int32_t *amcol = L.argmax + tc;
     // A warp whose rows all belong to queries no document scores with c != 0 stores zeros.
     const bool warp_idle = __all_sync(0xffffffffu, L.q_active != nullptr && L.q_active[q] == 0);
-    // The loads that resolve document d (its argmax entry and c) ...
-    int a_n = 0;
+    // The documents in turn: the active ones from the list when some are not (every other document has
+    // c = 0 for every query), else all of them in order (no list indirection in the loads).
+    const int n_docs = L.d_list ? static_cast<int>(*L.d_count) : L.nd;
+    const bool use_list = n_docs < L.nd;
+    // The loads that resolve the i-th document (its id, argmax entry and c) ...
+    int a_n = 0, d_n = 0;
     float c_n = 0.f;
-    auto fetch = [&](int d) {
-        if (d < L.nd) {
-            a_n = __ldg(amcol + static_cast<long long>(d) * L.ld_argmax);
-            c_n = __ldg(dsrow + d);
+    auto fetch = [&](int i) {
+        if (i < n_docs) {
+            d_n = use_list ? static_cast<int>(__ldg(L.d_list + i)) : i;
+            a_n = __ldg(amcol + static_cast<long long>(d_n) * L.ld_argmax);
+            c_n = __ldg(dsrow + d_n);
         }
     };
     // ... and their use, with the document's offsets (a small, cache-resident table): the gathered row
     // (the zero row past the last document, for a rejected entry or for c = 0) and c.
     const unsigned long long zero_row = reinterpret_cast<unsigned long long>(kZeroRow);
-    auto finish = [&](int d, unsigned long long &src, float &c) {
+    auto finish = [&](int i, unsigned long long &src, float &c) {
         src = zero_row;
         c = 0.f;
-        if (d < L.nd) {
+        if (i < n_docs) {
+            const int d = use_list ? d_n : i;   // in order, the offsets' addresses need no loaded value
             const uint64_t o = __ldg(L.d_off + d), e = __ldg(L.d_off + d + 1);
             if (a_n < 0 || static_cast<uint64_t>(a_n) >= e - o) {
                 if (row_ok) report(L.status, CLI_MALFORMED);
@@ -707,7 +713,7 @@ __global__ void __launch_bounds__(256, NBLK <= 2 ? 4 : 2) dq_kernel(MaxSimBwdLau
     float c;
     fetch(sub);
     finish(sub, src, c);
-    for (int d0 = 0; d0 < (warp_idle ? 0 : L.nd); d0 += kDqUnroll) {
+    for (int d0 = 0; d0 < (warp_idle ? 0 : n_docs); d0 += kDqUnroll) {
         fetch(d0 + kDqUnroll + sub);   // the next step's resolution, in flight during this step
         step(src, c);
         finish(d0 + kDqUnroll + sub, src, c);
@@ -1067,6 +1073,9 @@ cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream
             (err = cudaMemsetAsync(L.d_active, 0, L.nd, stream)) != cudaSuccess)
             return err;
         active_kernel<<<L.nq, 256, 0, stream>>>(L.d_scores, L.ld_ds, L.nd, L.q_active, L.d_active, L.status);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        compact_items_kernel<uint8_t><<<1, kCompactThreads, 0, stream>>>(L.d_active, L.nd, L.d_list, L.d_count,
+                                                                         L.status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
         dd_zero_kernel<<<L.nd, 512, 0, stream>>>(L);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
