@@ -548,22 +548,14 @@ __global__ void active_kernel(const float *d_scores, long long ld_ds, int nd, ui
     if (__syncthreads_or(any) && threadIdx.x == 0) q_active[q] = 1;
 }
 
-// The dD rows of a document no query scores are zero; its argmax entries are
-// still checked (active documents check theirs in dd_sort_kernel).
+// The dD rows of a document no query scores are zero (its argmax entries are
+// not read).
 __global__ void dd_zero_kernel(MaxSimBwdLaunch L) {
     if (read_status(L.status) != 0) return;
     const int d = blockIdx.x;
     if (L.d_active[d]) return;
     const uint64_t o0 = L.d_off[d];
     const int dl = static_cast<int>(L.d_off[d + 1] - o0);
-    const int32_t *am = L.argmax + static_cast<long long>(d) * L.ld_argmax;
-    bool bad = false;
-#pragma unroll 8
-    for (int k = threadIdx.x; k < L.rows_q; k += blockDim.x) {   // independent loads, one report at the end
-        const int a = __ldg(am + k);
-        bad |= a < 0 || a >= dl;
-    }
-    if (bad) report(L.status, CLI_MALFORMED);
     float4 *dst = reinterpret_cast<float4 *>(L.dd + static_cast<long long>(o0) * L.width);
     const long long n4 = static_cast<long long>(dl) * L.width / 4;
     for (long long i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -646,11 +638,13 @@ __global__ void __launch_bounds__(256, NBLK <= 2 ? 4 : 2) dq_kernel(MaxSimBwdLau
         if (i < n_docs) {
             const int d = use_list ? d_n : i;   // in order, the offsets' addresses need no loaded value
             const uint64_t o = __ldg(L.d_off + d), e = __ldg(L.d_off + d + 1);
-            if (a_n < 0 || static_cast<uint64_t>(a_n) >= e - o) {
-                if (row_ok) report(L.status, CLI_MALFORMED);
-            } else if (c_n != 0.0f) {   // a pair with c = 0 (one a loss ignores) gathers nothing
-                src = reinterpret_cast<unsigned long long>(L.d + (o + static_cast<uint64_t>(a_n)) * L.width);
-                c = c_n * scale;
+            if (c_n != 0.0f) {   // a pair with c = 0 (one a loss ignores) gathers nothing, nor is checked
+                if (a_n < 0 || static_cast<uint64_t>(a_n) >= e - o) {
+                    if (row_ok) report(L.status, CLI_MALFORMED);
+                } else {
+                    src = reinterpret_cast<unsigned long long>(L.d + (o + static_cast<uint64_t>(a_n)) * L.width);
+                    c = c_n * scale;
+                }
             }
         }
     };
@@ -853,11 +847,11 @@ __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch 
 #pragma unroll
                 for (int i = 0; i < kDsBatch; ++i) {
                     if (k0 + i * kDsThreads >= crows) break;
+                    if (skip_zero && ctab[qv[i]] == 0.0f) continue;   // adds nothing to dD, and is not read
                     if (a[i] < 0 || a[i] >= dl) {
                         report(L.status, CLI_MALFORMED);
                         continue;
                     }
-                    if (skip_zero && ctab[qv[i]] == 0.0f) continue;   // adds nothing to dD
                     const int r = a[i] - w0;
                     if (r >= 0 && r < wrows) atomicAdd(&cnt[r], 1u);
                 }

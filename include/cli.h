@@ -29,7 +29,8 @@
  *     pointer) returns a status synchronously and enqueues nothing.
  *   - A fault only the device can see (offsets that decrease or run past the
  *     data, ids out of range or not strictly ascending, an empty query or
- *     document, an argmax entry outside its document) is written to the
+ *     document, an argmax entry outside its document where the backward reads
+ *     it, i.e. for a pair with c != 0) is written to the
  *     caller-lent `device_status` word (0 = success) by a validation kernel
  *     that runs first on the stream; the compute kernels then do nothing and
  *     the outputs are unspecified.  Nothing ever traps.  A device wait that
@@ -354,15 +355,17 @@ size_t maxsim_named_workspace_bytes(size_t query_count, size_t document_count, s
  *     dQ[t]      += c * D[offsets_d + argmax[d][t]]
  *     dD[offsets_d + argmax[d][t]] += c * Q[t].
  *
- *   argmax        device int32, the layout maxsim_scores writes
+ *   argmax        device int32, the layout maxsim_scores writes; an entry of a
+ *                 pair with c = 0 is not read (nor checked)
  *   d_scores      device fp32 [queries.count x ld_d_scores]
  *   d_queries     device fp32 [queries.rows x width] (written)
  *   d_documents   device fp32 [documents.rows x width] (written)
  *   workspace     device, >= maxsim_backward_workspace_bytes(...), 256-byte
- *                 aligned: the row -> query map and one flag per query and
- *                 per document (whether some c is nonzero: the rows of a
- *                 query or document with c = 0 throughout are written as
- *                 zeros without gathering); contents on entry are ignored
+ *                 aligned: the row -> query map, one flag per query and per
+ *                 document (whether some c is nonzero: the rows of a query or
+ *                 document with c = 0 throughout are written as zeros without
+ *                 gathering), and the list of active documents; contents
+ *                 on entry are ignored
  */
 typedef struct {
     cli_tape_t queries, documents;

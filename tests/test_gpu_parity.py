@@ -230,9 +230,13 @@ def test_maxsim_device_faults_are_reported():
     assert int(f["device_status"].item()) == 5
     f = cli.maxsim_scores(q, qo, d, do)
     am = f["argmax"].clone()
-    am[2, 7] = 32                            # outside its document
-    g = cli.maxsim_backward(q, qo, d, do, am, torch.zeros(16, 16, device=dev()))
+    am[2, 7] = 32                            # outside its document (row 7 is query 0's)
+    ds = torch.ones(16, 16, device=dev())
+    g = cli.maxsim_backward(q, qo, d, do, am, ds)
     assert int(g["device_status"].item()) == 5
+    ds[0, 2] = 0.0                           # the entry's pair has c = 0: it is not read, nor checked
+    g = cli.maxsim_backward(q, qo, d, do, am, ds)
+    assert int(g["device_status"].item()) == 0
 
 
 # ---------------------------------------------------------------------------
