@@ -175,6 +175,36 @@ def test_maxsim_backward_routes_a_given_argmax():
     assert rel_l2(g["dd"], dd) <= 1e-5
 
 
+@pytest.mark.parametrize("mean", [False, True])
+def test_maxsim_backward_skips_inactive_queries_and_documents(mean):
+    """dS with whole rows (queries) and columns (documents) zero, as a loss that ignores them gives: the
+    backward skips those queries' warps and documents' blocks and walks the list of active documents; dQ
+    and dD (zeros included) equal the oracle's routing of the same argmax, and an argmax entry that
+    only zero-c pairs would read is not checked."""
+    m = synth.maxsim_random(8, 90, 70, 128, (3, 50), (5, 260))
+    am = synth.random_argmax(9, m)
+    ds = np.array(m.d_scores, dtype=np.float32)
+    rng = np.random.default_rng(10)
+    dead_q = rng.random(m.nq) < 0.35
+    dead_d = rng.random(m.nd) < 0.35
+    ds[dead_q, :] = 0.0
+    ds[:, dead_d] = 0.0
+    d0 = int(np.nonzero(dead_d)[0][0])
+    am[d0, 0] = 10 ** 6                      # outside its document, but only zero-c pairs would read it
+    q, qo, d, do = bf16(m.q_bf16), i64(m.q_offsets), bf16(m.d_bf16), i64(m.d_offsets)
+    g = cli.maxsim_backward(q, qo, d, do, torch.from_numpy(am).to(dev()), torch.from_numpy(ds).to(dev()),
+                            mean=mean)
+    torch.cuda.synchronize()
+    assert int(g["device_status"].item()) == 0
+    am[d0, 0] = 0
+    dq, dd = oracle.maxsim_backward(m.q_offsets, m.q, m.d_offsets, m.d, am, ds.astype(np.float64), mean)
+    gq, gd = g["d_queries"].double().cpu().numpy(), g["d_documents"].double().cpu().numpy()
+    assert rel_l2(gq, dq) <= 1e-5 and rel_l2(gd, dd) <= 1e-5
+    rq = np.repeat(np.arange(m.nq), np.diff(m.q_offsets.astype(np.int64)))
+    rd = np.repeat(np.arange(m.nd), np.diff(m.d_offsets.astype(np.int64)))
+    assert np.all(gq[dead_q[rq]] == 0.0) and np.all(gd[dead_d[rd]] == 0.0)
+
+
 def test_maxsim_copied_queries_find_themselves():
     """A query made of rows copied from a document matches them exactly there (config-5 structure)."""
     j = synth.joint(0, pooled_count=256, pooled_width=64, items=24, d_len=(8, 40), q_len=(2, 8))
