@@ -218,6 +218,12 @@ __device__ __forceinline__ float fast_rcp(float x) {
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// Three-input minimum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 
 // sigma(z), sigma(-z) and softplus(z) from one exp(-|z|):
 //   e = exp(-|z|), sigma(z) = 1/(1+e) for z >= 0 and e/(1+e) otherwise,
@@ -572,17 +578,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float fix_l = 0.f, fix_g = 0.f, fix_gs = 0.f;   // corrections for special cells
 #pragma unroll 1
                 for (int ch = 0; ch < BM / 32; ++ch) {
-                    float v[32];
-                    tmem_ld32(tmem + lane_base + slot * BM + ch * 32, v);
+                    // The chunk's scores and their maximum (a reducing TMEM load), and their minimum (a
+                    // tree of three-input min operations): the chunk's range of z (t may be negative)
+                    // picks the cheapest exact-enough path.
+                    float v[32], smax;
+                    {
+                        uint32_t r[32];
+                        tmem_ld32_max_async(tmem + lane_base + slot * BM + ch * 32, r, smax);
+                        tmem_wait_ld();
+                        tmem_regs_ready(r, smax);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                    }
+                    float m3[11];
+#pragma unroll
+                    for (int i = 0; i < 10; ++i) m3[i] = fmin3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+                    m3[10] = fminf(v[30], v[31]);
+                    const float smin = fminf(fmin3(fmin3(m3[0], m3[1], m3[2]), fmin3(m3[3], m3[4], m3[5]),
+                                                   fmin3(m3[6], m3[7], m3[8])),
+                                             fmin3(m3[9], m3[10], m3[10]));
                     const int c0 = j0 + ch * 32;
                     const int valid = min(32, P.n - c0);   // columns of this chunk inside the batch
-                    // The chunk's range of z (t may be negative) picks the cheapest exact-enough path.
-                    float smin = v[0], smax = v[0];
-#pragma unroll
-                    for (int r = 1; r < 32; ++r) {
-                        smin = fminf(smin, v[r]);
-                        smax = fmaxf(smax, v[r]);
-                    }
                     const float za = fmaf(t, smin, b), zb = fmaf(t, smax, b);
                     const float zlo = fminf(za, zb), zhi = fmaxf(za, zb);
                     float hv[32];
