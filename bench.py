@@ -457,23 +457,31 @@ def peaks():
     return 1900.0, 1700.0, 6800.0, "fallback"
 
 
-def kernel_source_hash():
+# Committed DRAM-traffic records: file under profiles/ -> the kernel sources its counters were taken on.
+TRAFFIC_RECORDS = {
+    "maxsim": ("maxsim_forward_traffic.json", ("maxsim.cu", "cli_device.cuh")),
+    "pooled": ("pooled_fused_traffic.json", ("pair_loss.cu", "cli_device.cuh")),
+}
+
+
+def kernel_source_hash(files=TRAFFIC_RECORDS["maxsim"][1]):
     h = hashlib.sha256()
-    for name in ("maxsim.cu", "cli_device.cuh"):
+    for name in files:
         with open(os.path.join(ROOT, "contrastive_late_interaction_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(workload):
-    """DRAM bytes per launch of the MaxSim forward kernel from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "maxsim_forward_traffic.json")
+def committed_traffic(workload, kind="maxsim"):
+    """DRAM bytes per launch of the roofline kernel (the MaxSim forward tile kernel, or the pooled fused block
+    kernel) from the committed ncu summary, if it was taken on the current kernel source; else None."""
+    record, files = TRAFFIC_RECORDS[kind]
+    path = os.path.join(ROOT, "profiles", record)
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    if d.get("source_hash") != kernel_source_hash():
+    if d.get("source_hash") != kernel_source_hash(files):
         return None
     return d.get("per_launch_bytes", {}).get(workload)
 
@@ -697,7 +705,7 @@ def main():
                 "pair_loss_sigmoid_matryoshka_fwd_bwd" if pre else "pair_loss_sigmoid_fwd_bwd")
         roofline = {"kernel": f"pooled fused block kernel ({call} call)", "bound": "tensor",
                     "achieved": achieved, "peak": sustained, "unit": "TFLOP/s", "frac": achieved / sustained,
-                    "peak_source": f"{peak_src} bf16 sustained", "traffic": None,
+                    "peak_source": f"{peak_src} bf16 sustained", "traffic": committed_traffic(args.workload, "pooled"),
                     "algorithmic_per_launch": pooled_flops(p, pre)}
 
     # end to end through the C ABI with host buffers: inputs copied in, losses read back, every step
