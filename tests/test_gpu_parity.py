@@ -49,7 +49,8 @@ def test_pooled_config2_full():
     compare_pooled(p, g, ref)
 
 
-@pytest.mark.parametrize("n,width,named", [(300, 72, False), (129, 8, True), (1000, 200, False), (2, 64, False)])
+@pytest.mark.parametrize("n,width,named", [(300, 72, False), (129, 8, True), (1000, 200, False), (2, 64, False),
+                                            (200, 1024, False), (130, 4096, True)])   # up to the widest width
 def test_pooled_ragged_weighted(n, width, named):
     """Ragged tiles (N and D not multiples of the tile), weighted attract and repel edges, ignores,
     both negatives modes, padded input and output row strides."""
@@ -159,6 +160,8 @@ def test_maxsim_tiny(mean):
     (4, 300, 3, 8, (1, 3), (1000, 1300)),     # width 8
     (6, 5000, 3, 64, (1, 2), (5, 40)),        # more queries than the backward's shared table of c(q, d)
     (7, 70000, 2, 64, (1, 1), (3, 20)),       # more queries than its list entries can name
+    (8, 6, 3, 128, (5, 40), (5000, 9000)),    # documents longer than the backward's 4096-row window
+    (9, 4, 2, 64, (8, 16), (70000, 70000)),   # argmax indices past 16 bits
 ])
 def test_maxsim_ragged(seed, nq, nd, width, ql, dl):
     compare_maxsim_full(synth.maxsim_random(seed, nq, nd, width, ql, dl))
