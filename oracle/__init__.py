@@ -168,7 +168,7 @@ def _dense_relations(n, attract, repel, ignore, negatives_named, ambient_weight)
 
 
 def pair_loss_sigmoid_groups(e, groups, t, b, attract=None, repel=None, ignore=None, negatives_named=False,
-                             ambient_weight=1.0):
+                             ambient_weight=1.0, band=None):
     """Pooled sigmoid pair loss with temperature groups.  Returns dict(loss, dt, db, de) with dt, db one per
     group.
 
@@ -177,12 +177,23 @@ def pair_loss_sigmoid_groups(e, groups, t, b, attract=None, repel=None, ignore=N
     anchor's pair: z_ij = t[g(i)] s_ij + b[g(i)], l_ij = w_ij softplus(-y_ij z_ij), L = (1/N) sum l_ij
     (the SigLIP loss of "UForm", section "Matryoshka-Like Multi-Scale Embedders", per anchor).  Written out
     densely in float64 (a second formulation beside the C oracle, which it equals with one group).
+
+    `band` = (row_begin, row_count) keeps only the cells whose anchor i lies in those rows, still divided
+    by N: one device's share when the loss is sharded by rows ("UForm", section "NVLink-Based Cross-GPU
+    Collaboration": each device scores its band of rows against every column, and the gradients are
+    reduce-scattered), so the shares of bands that partition the rows add up to the whole.
     """
     e = _f64(e)
     n = e.shape[0]
     g = np.asarray(groups, dtype=np.int64)
     tv, bv = np.asarray(t, dtype=np.float64), np.asarray(b, dtype=np.float64)
     Y, W = _dense_relations(n, attract, repel, ignore, negatives_named, ambient_weight)
+    if band is not None:
+        lo, count = int(band[0]), int(band[1])
+        outside = np.ones(n, dtype=bool)
+        outside[lo:lo + count] = False
+        W[outside, :] = 0.0
+        Y[outside, :] = 0
     S = e @ e.T
     Z = tv[g][:, None] * S + bv[g][:, None]
     m = -Y * Z                                    # softplus(-y z) and its derivative sigma(-y z)

@@ -110,3 +110,74 @@ def test_finite_differences():
         bm[q] -= h
         assert (loss(e, tp, b) - loss(e, tm, b)) / (2 * h) == pytest.approx(base["dt"][q], rel=1e-6, abs=1e-9)
         assert (loss(e, t, bp) - loss(e, t, bm)) / (2 * h) == pytest.approx(base["db"][q], rel=1e-6, abs=1e-9)
+
+
+# ---------------------------------------------------------------------------
+# Anchor bands: one device's rows when the loss is sharded by rows ("UForm", section "NVLink-Based
+# Cross-GPU Collaboration": each device scores its band of rows against every column).
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("named", [False, True])
+def test_band_shares_are_the_c_oracles_anchor_rows(named):
+    """The C oracle evaluates listed anchors' rows on its own: a band's L, dt, db must be those rows'
+    shares (this separates a band of rows from a band of columns)."""
+    rng = np.random.default_rng(11 + named)
+    n = 13
+    e = rng.normal(size=(n, 6))
+    att, rep, ign = random_relations(rng, n)
+    for lo, cnt in ((0, 4), (4, 1), (5, 8)):
+        a = oracle.pair_loss_sigmoid_groups(e, np.zeros(n, int), [2.0], [-1.0], att, rep, ign, named, 0.8,
+                                            band=(lo, cnt))
+        c = oracle.pair_loss_sigmoid(e, 2.0, -1.0, att, rep, ign, named, 0.8, rows=np.arange(lo, lo + cnt))
+        assert a["loss"] == pytest.approx(c["loss"], rel=1e-12)
+        assert a["dt"][0] == pytest.approx(c["dt"], rel=1e-11, abs=1e-15)
+        assert a["db"][0] == pytest.approx(c["db"], rel=1e-11, abs=1e-15)
+
+
+def test_bands_that_partition_the_rows_add_up():
+    rng = np.random.default_rng(21)
+    n = 11
+    e = rng.normal(size=(n, 4))
+    att, rep, ign = random_relations(rng, n)
+    g = rng.integers(0, 3, size=n)
+    t, b = np.array([1.5, -0.5, 2.5]), np.array([0.2, 0.7, -1.1])
+    full = oracle.pair_loss_sigmoid_groups(e, g, t, b, att, rep, ign, False, 0.9)
+    parts = [oracle.pair_loss_sigmoid_groups(e, g, t, b, att, rep, ign, False, 0.9, band=bd)
+             for bd in ((0, 3), (3, 5), (8, 3))]
+    assert sum(p["loss"] for p in parts) == pytest.approx(full["loss"], rel=1e-12)
+    np.testing.assert_allclose(sum(p["dt"] for p in parts), full["dt"], rtol=1e-11, atol=1e-15)
+    np.testing.assert_allclose(sum(p["db"] for p in parts), full["db"], rtol=1e-11, atol=1e-15)
+    np.testing.assert_allclose(sum(p["de"] for p in parts), full["de"], rtol=1e-11, atol=1e-14)
+    # a band's gradient reaches rows outside it (through the columns its anchors score)
+    assert np.abs(parts[0]["de"][3:]).max() > 0
+
+
+def test_band_finite_differences():
+    """A band's dE, dt and db are the gradients of that band's loss share."""
+    rng = np.random.default_rng(31)
+    n, w = 7, 4
+    e = rng.normal(size=(n, w))
+    att, rep, ign = random_relations(rng, n)
+    g = np.array([0, 1, 1, 0, 1, 0, 1])
+    t, b = np.array([1.5, -0.5]), np.array([0.2, 0.7])
+    band = (2, 3)
+    base = oracle.pair_loss_sigmoid_groups(e, g, t, b, att, rep, ign, False, 0.9, band=band)
+
+    def loss(e_, t_, b_):
+        return oracle.pair_loss_sigmoid_groups(e_, g, t_, b_, att, rep, ign, False, 0.9, band=band)["loss"]
+
+    h = 1e-6
+    for i in range(n):
+        for k in range(w):
+            ep, em = e.copy(), e.copy()
+            ep[i, k] += h
+            em[i, k] -= h
+            assert (loss(ep, t, b) - loss(em, t, b)) / (2 * h) == pytest.approx(base["de"][i, k], rel=1e-6, abs=1e-9)
+    for q in range(2):
+        tp, tm, bp, bm = t.copy(), t.copy(), b.copy(), b.copy()
+        tp[q] += h
+        tm[q] -= h
+        bp[q] += h
+        bm[q] -= h
+        assert (loss(e, tp, b) - loss(e, tm, b)) / (2 * h) == pytest.approx(base["dt"][q], rel=1e-6, abs=1e-9)
+        assert (loss(e, t, bp) - loss(e, t, bm)) / (2 * h) == pytest.approx(base["db"][q], rel=1e-6, abs=1e-9)
