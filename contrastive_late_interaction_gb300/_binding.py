@@ -82,7 +82,8 @@ class PairLossSigmoidArgs(ctypes.Structure):
                 ("inverse_temperature", c_void_p), ("bias", c_void_p), ("relations", Relations),
                 ("loss", c_void_p), ("d_embeddings", c_void_p), ("ld_d_embeddings", c_size_t),
                 ("d_inverse_temperature", c_void_p), ("d_bias", c_void_p), ("workspace", c_void_p),
-                ("workspace_bytes", c_size_t), ("device_status", c_void_p), ("stream", c_void_p)]
+                ("workspace_bytes", c_size_t), ("device_status", c_void_p), ("stream", c_void_p),
+                ("row_begin", c_size_t), ("row_count", c_size_t)]
 
 
 class PairLossGroupsArgs(ctypes.Structure):
@@ -232,6 +233,16 @@ def device_edges(edges, device="cuda"):
     return (o, i, ww) if ww is not None else (o, i)
 
 
+def _band(band):
+    """The anchor band (row_begin, row_count) of a pooled call; None is every row.  The library checks it."""
+    if band is None:
+        return dict(row_begin=0, row_count=0)
+    begin, count = (int(v) for v in band)
+    if begin < 0 or count < 0:
+        raise ShapeMismatchError(CLI_SHAPE_MISMATCH, "band must be (row_begin, row_count) >= 0")
+    return dict(row_begin=begin, row_count=count)
+
+
 def _ws(nbytes, device):
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
@@ -251,10 +262,11 @@ def pair_loss_sigmoid_workspace_bytes(count, width, edges):
 
 def pair_loss_sigmoid_fwd_bwd(embeddings, inverse_temperature, bias, attract, repel=None, ignore=None,
                               negatives_named=False, ambient_weight=1.0, out=None, workspace=None,
-                              device_status=None, stream=None):
+                              device_status=None, stream=None, band=None):
     """Pooled sigmoid pair loss over bf16 embeddings [N, ld] (first `width` = embeddings.shape[1] columns
     unless `out['width']` narrows it).  Returns dict(loss, d_embeddings, d_inverse_temperature, d_bias,
-    device_status) of device tensors; the device status is not synchronised here."""
+    device_status) of device tensors; the device status is not synchronised here.  `band` = (row_begin,
+    row_count) scores only the anchors in those rows: the results are that band's shares of the whole call's."""
     _check_cuda(embeddings, "embeddings", torch.bfloat16)
     _check_cuda(inverse_temperature, "inverse_temperature", torch.float32)
     _check_cuda(bias, "bias", torch.float32)
@@ -277,14 +289,14 @@ def pair_loss_sigmoid_fwd_bwd(embeddings, inverse_temperature, bias, attract, re
         relations=Relations(A, R, I, int(bool(negatives_named)), float(ambient_weight)),
         loss=_ptr(loss), d_embeddings=_ptr(de), ld_d_embeddings=de.stride(0),
         d_inverse_temperature=_ptr(dt), d_bias=_ptr(db), workspace=_ptr(ws), workspace_bytes=ws.numel(),
-        device_status=_ptr(st), stream=_stream(stream))
+        device_status=_ptr(st), stream=_stream(stream), **_band(band))
     raise_for(lib.pair_loss_sigmoid_fwd_bwd(ctypes.byref(args)), "pair_loss_sigmoid_fwd_bwd")
     return dict(loss=loss, d_embeddings=de, d_inverse_temperature=dt, d_bias=db, device_status=st)
 
 
 def pair_loss_sigmoid_groups_fwd_bwd(embeddings, groups, inverse_temperature, bias, attract, repel=None, ignore=None,
                                      negatives_named=False, ambient_weight=1.0, out=None, workspace=None,
-                                     device_status=None, stream=None):
+                                     device_status=None, stream=None, band=None):
     """The pooled sigmoid pair loss with temperature groups: `groups` (int32 [N]) selects each item's pair of
     `inverse_temperature`, `bias` (fp32 [G]) and a cell takes its anchor's.  Returns dict(loss, d_embeddings,
     d_inverse_temperature [G], d_bias [G], device_status) of device tensors."""
@@ -314,7 +326,7 @@ def pair_loss_sigmoid_groups_fwd_bwd(embeddings, groups, inverse_temperature, bi
         relations=Relations(A, R, I, int(bool(negatives_named)), float(ambient_weight)),
         loss=_ptr(loss), d_embeddings=_ptr(de), ld_d_embeddings=de.stride(0),
         d_inverse_temperature=_ptr(dt), d_bias=_ptr(db), workspace=_ptr(ws), workspace_bytes=ws.numel(),
-        device_status=_ptr(st), stream=_stream(stream))
+        device_status=_ptr(st), stream=_stream(stream), **_band(band))
     args = PairLossGroupsArgs(base=base, groups=_ptr(groups), group_count=g)
     raise_for(lib.pair_loss_sigmoid_groups_fwd_bwd(ctypes.byref(args)), "pair_loss_sigmoid_groups_fwd_bwd")
     return dict(loss=loss, d_embeddings=de, d_inverse_temperature=dt, d_bias=db, device_status=st)
@@ -326,7 +338,7 @@ def pair_loss_sigmoid_matryoshka_workspace_bytes(count, width, edges):
 
 def pair_loss_sigmoid_matryoshka_fwd_bwd(embeddings, prefix_widths, inverse_temperature, bias, attract, repel=None,
                                          ignore=None, negatives_named=False, ambient_weight=1.0, out=None,
-                                         workspace=None, device_status=None, stream=None):
+                                         workspace=None, device_status=None, stream=None, band=None):
     """The pooled sigmoid pair loss summed over the normalised prefixes `prefix_widths` of bf16 embeddings
     [N, ld] (first `width` = embeddings.shape[1] columns unless `out['width']` narrows it).  Returns
     dict(loss, d_embeddings, d_inverse_temperature, d_bias, prefix_loss, device_status) of device tensors."""
@@ -355,7 +367,7 @@ def pair_loss_sigmoid_matryoshka_fwd_bwd(embeddings, prefix_widths, inverse_temp
         relations=Relations(A, R, I, int(bool(negatives_named)), float(ambient_weight)),
         loss=_ptr(loss), d_embeddings=_ptr(de), ld_d_embeddings=de.stride(0),
         d_inverse_temperature=_ptr(dt), d_bias=_ptr(db), workspace=_ptr(ws), workspace_bytes=ws.numel(),
-        device_status=_ptr(st), stream=_stream(stream))
+        device_status=_ptr(st), stream=_stream(stream), **_band(band))
     args = PairLossMatryoshkaArgs(base=base, prefix_widths=ctypes.cast(widths, c_void_p),
                                   prefix_count=len(prefix_widths), prefix_loss=_ptr(pl))
     raise_for(lib.pair_loss_sigmoid_matryoshka_fwd_bwd(ctypes.byref(args)), "pair_loss_sigmoid_matryoshka_fwd_bwd")

@@ -110,6 +110,8 @@ cli_status_t pooled_checks(const cli_pair_loss_sigmoid_t *a, size_t &edges) {
     if (a->count < 2 || a->count >= (1ull << 31)) return CLI_SHAPE_MISMATCH;
     if (a->width == 0 || a->width % 8 != 0 || a->ld < a->width || a->ld % 8 != 0) return CLI_SHAPE_MISMATCH;
     if (a->width > 4096) return CLI_UNSUPPORTED;
+    if (a->row_begin > a->count || a->row_count > a->count - a->row_begin) return CLI_SHAPE_MISMATCH;
+    if (a->row_count == 0 && a->row_begin != 0) return CLI_SHAPE_MISMATCH;
     if (a->ld_d_embeddings < a->width || a->ld_d_embeddings % 4 != 0) return CLI_SHAPE_MISMATCH;
     if (!aligned(a->embeddings, 16) || !aligned(a->d_embeddings, 16) || !aligned(a->workspace, 256))
         return CLI_INVALID_ARGUMENT;
@@ -178,6 +180,8 @@ PooledLaunch pooled_launch_record(const cli_pair_loss_sigmoid_t *a, const Pooled
     L.db = db;
     L.status = a->device_status;
     L.sm_count = sms;
+    L.row_lo = static_cast<int>(a->row_begin);
+    L.row_hi = a->row_count ? static_cast<int>(a->row_begin + a->row_count) : 0;
     return L;
 }
 

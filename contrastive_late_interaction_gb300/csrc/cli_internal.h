@@ -63,6 +63,9 @@ struct PooledLaunch {
     // (t, b).  With groups, t_ptr and b_ptr index by group and dt, db are
     // per-group arrays that the kernel adds into (zeroed by the caller).
     const int32_t *group = nullptr;
+    // Anchor band: only cells whose row (anchor) lies in row_lo .. row_hi - 1
+    // are scored (row_hi = 0: every row).
+    int row_lo = 0, row_hi = 0;
 };
 
 // Relation preparation: validation, transposition and merged special lists.

@@ -96,6 +96,10 @@ struct Params {
     // the per-group gradients (accumulated), and the mode's full grid of blocks.
     const int32_t *group;
     float *dt_g, *db_g;
+    // Ordered traversal (groups, or an anchor band): every block (I, J) of block
+    // rows bi0 .. bi0 + blocks / nbb - 1, each cell scored for its row's anchor
+    // only, and only anchors in rows row_lo .. row_hi - 1.
+    int ordered, bi0, row_lo, row_hi;
 };
 
 // Pair p -> (I, J), I <= J, over an n x n grid.  The upper triangle is walked
@@ -164,8 +168,8 @@ struct Block {
 
 __device__ __forceinline__ Block decode_block(long long p, const Params &P) {
     int bi, bj;
-    if (P.group) {   // every ordered block, each cell scored for its row's anchor only
-        bi = static_cast<int>(p / P.nbb);
+    if (P.ordered) {   // every ordered block, each cell scored for its row's anchor only
+        bi = P.bi0 + static_cast<int>(p / P.nbb);
         bj = static_cast<int>(p % P.nbb);
     } else {
         decode_pair(p, P.nbb, bi, bj);
@@ -173,7 +177,7 @@ __device__ __forceinline__ Block decode_block(long long p, const Params &P) {
     Block b;
     b.I0 = 2 * bi;
     b.J0 = 2 * bj;
-    b.diag = bi == bj && !P.group;
+    b.diag = bi == bj && !P.ordered;
     b.i1 = b.I0 + 1 < P.nb;
     b.j1 = b.J0 + 1 < P.nb;
     return b;
@@ -538,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv_n = 1.0f / static_cast<float>(P.n);
         const float w_d = P.named ? 0.0f : P.ambient;
         // A visited cell serves both ordered pairs, or (with groups) its row's anchor only.
-        const float dirs = P.group ? 1.0f : 2.0f;
+        const float dirs = P.ordered ? 1.0f : 2.0f;
         const float w_dd = dirs * w_d;
         const uint32_t stage_s = smem_u32(sm.stage_t[ew]);
         uint32_t kblk = 0, chunk = 0;
@@ -546,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Block bk = decode_block(p, P);
             const bool x_on = x == 0 || bk.i1;
             const int gi = (bk.I0 + x) * BM + row;   // this thread's item (anchor)
-            const bool row_ok = x_on && gi < P.n;
+            const bool row_ok = x_on && gi >= P.row_lo && gi < P.row_hi;
             const int y_first = (bk.diag && x == 1) ? 1 : 0;
             // This row's (t, b): the run's pair, or its anchor's group's.
             const int grp = (P.group && row_ok) ? P.group[gi] : 0;
@@ -628,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float z = fmaf(t, s, b);
                         const CellFn f = cell_fn(z);
                         const bool ao = en.flags & 1u, ai = en.flags & 2u;
-                        const float w_in = P.group ? 0.0f : en.w_in;   // (j, i) is its own visit with groups
+                        const float w_in = P.ordered ? 0.0f : en.w_in;   // (j, i) is its own visit when ordered
                         const float g = en.w_out * (ao ? -f.pc : f.p) + w_in * (ai ? -f.pc : f.p);
                         const float l = en.w_out * (ao ? f.sp - z : f.sp) + w_in * (ai ? f.sp - z : f.sp);
                         const float g_def = w_dd * f.p;
@@ -779,7 +783,8 @@ __global__ void finish_kernel(const double *sums, int n, float *loss, float *dt,
     }
 }
 
-// Blocks of one call: the upper triangle, or every ordered block with groups.
+// Blocks of one call: the upper triangle, or every ordered block (groups, or an
+// anchor band covering the whole batch at most).
 long long block_count(int n, bool groups) {
     const long long nb = (n + BM - 1) / BM, nbb = (nb + 1) / 2;
     return groups ? nbb * nbb : nbb * (nbb + 1) / 2;
@@ -807,7 +812,14 @@ cudaError_t launch_pooled_fused(const CUtensorMap &tmap_e, const PooledLaunch &L
     P.nk = (L.width + BK - 1) / BK;
     P.nb = (L.n + BM - 1) / BM;
     P.nbb = (P.nb + 1) / 2;
-    P.blocks = block_count(L.n, L.group != nullptr);
+    // An anchor band narrower than the batch takes the ordered traversal over the block rows it touches.
+    P.row_lo = L.row_lo;
+    P.row_hi = L.row_hi > 0 ? L.row_hi : L.n;
+    const bool band = P.row_lo > 0 || P.row_hi < L.n;
+    P.ordered = (L.group != nullptr || band) ? 1 : 0;
+    P.bi0 = P.ordered ? P.row_lo / (2 * BM) : 0;
+    const long long bi_end = P.ordered ? (P.row_hi + 2 * BM - 1) / (2 * BM) : 0;
+    P.blocks = P.ordered ? (bi_end - P.bi0) * P.nbb : block_count(L.n, false);
     P.group = L.group;
     P.dt_g = L.group ? L.dt : nullptr;
     P.db_g = L.group ? L.db : nullptr;
@@ -821,6 +833,7 @@ cudaError_t launch_pooled_fused(const CUtensorMap &tmap_e, const PooledLaunch &L
     P.ld_de = L.ld_de;
     P.partials = L.partials;
     P.status = L.status;
+    if (P.blocks <= 0) return cudaErrorInvalidValue;   // the host checks keep the band inside the batch
     long long grid = static_cast<long long>(L.sm_count);
     if (grid > P.blocks) grid = P.blocks;
     fused_blocks_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tmap_e, P);

@@ -116,6 +116,17 @@ typedef struct {
  *                   256-byte aligned; contents on entry are ignored
  *   device_status   device int32 (written: 0 or a cli_status_t)
  *   stream          cudaStream_t
+ *   row_begin, row_count   the anchor band: only ordered pairs (i, j) with
+ *                   row_begin <= i < row_begin + row_count are scored, and
+ *                   L, dL/dt, dL/db and dE (over all N rows) are that band's
+ *                   shares, still divided by N, so the results of bands that
+ *                   partition 0 .. N-1 add up to the whole call's.  This is
+ *                   one device's part when the loss is sharded by rows
+ *                   ("UForm", section "NVLink-Based Cross-GPU Collaboration":
+ *                   each device scores its band of rows against the gathered
+ *                   columns, and the gradients are reduce-scattered).  (0, 0):
+ *                   every row.  A band past the batch, or row_count = 0 with
+ *                   row_begin > 0, is CLI_SHAPE_MISMATCH.
  *
  * dE sums tile contributions with reductions in whatever order the GPU runs
  * them, so it is reproducible to rounding, not bit for bit; L, dt and db are
@@ -136,6 +147,7 @@ typedef struct {
     size_t workspace_bytes;
     int32_t *device_status;
     void *stream;
+    size_t row_begin, row_count;
 } cli_pair_loss_sigmoid_t;
 
 cli_status_t pair_loss_sigmoid_fwd_bwd(const cli_pair_loss_sigmoid_t *args);

@@ -88,6 +88,12 @@ def test_pooled_host_checks(b):
     assert call_pooled(b, ld_d_embeddings=510) == b.CLI_SHAPE_MISMATCH
     assert call_pooled(b, embeddings=A + 8) == b.CLI_INVALID_ARGUMENT               # not 16-byte aligned
     assert call_pooled(b, workspace_bytes=1024) == b.CLI_INVALID_ARGUMENT          # workspace too small
+    # the anchor band must lie inside the batch; (0, 0) is every row
+    assert call_pooled(b, row_begin=1000, row_count=25) == b.CLI_SHAPE_MISMATCH
+    assert call_pooled(b, row_begin=2**64 - 1, row_count=2) == b.CLI_SHAPE_MISMATCH
+    assert call_pooled(b, row_begin=5, row_count=0) == b.CLI_SHAPE_MISMATCH
+    assert call_pooled(b, row_begin=1000, row_count=24, workspace_bytes=1024) == b.CLI_INVALID_ARGUMENT
+    assert call_pooled(b, row_begin=0, row_count=0, workspace_bytes=1024) == b.CLI_INVALID_ARGUMENT
     # a step naming no attract edge is refused
     no_attract = b.Relations(b.Edges(None, None, None, 0), b.Edges(A * 4, A * 5, None, 7),
                              b.Edges(None, None, None, 0), 0, 1.0)
