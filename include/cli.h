@@ -121,10 +121,12 @@ typedef struct {
  *                   L, dL/dt, dL/db and dE (over all N rows) are that band's
  *                   shares, still divided by N, so the results of bands that
  *                   partition 0 .. N-1 add up to the whole call's.  This is
- *                   one device's part when the loss is sharded by rows
- *                   ("UForm", section "NVLink-Based Cross-GPU Collaboration":
- *                   each device scores its band of rows against the gathered
- *                   columns, and the gradients are reduce-scattered).  (0, 0):
+ *                   one device's part when the loss is sharded across
+ *                   devices ("UForm", section "Matryoshka-Like Multi-Scale
+ *                   Embedders": the per-rank embeddings all-gathered into
+ *                   one similarity band, the gradients reduce-scattered
+ *                   back), read as each rank scoring its own items' rows
+ *                   against every gathered column.  (0, 0):
  *                   every row.  A band past the batch, or row_count = 0 with
  *                   row_begin > 0, is CLI_SHAPE_MISMATCH.
  *

@@ -179,9 +179,11 @@ def pair_loss_sigmoid_groups(e, groups, t, b, attract=None, repel=None, ignore=N
     densely in float64 (a second formulation beside the C oracle, which it equals with one group).
 
     `band` = (row_begin, row_count) keeps only the cells whose anchor i lies in those rows, still divided
-    by N: one device's share when the loss is sharded by rows ("UForm", section "NVLink-Based Cross-GPU
-    Collaboration": each device scores its band of rows against every column, and the gradients are
-    reduce-scattered), so the shares of bands that partition the rows add up to the whole.
+    by N: one device's share when the loss is sharded across devices ("UForm", section "Matryoshka-Like
+    Multi-Scale Embedders": one SigLIP loss over the NVLink domain, the per-rank embeddings all-gathered
+    into one similarity band and the gradients reduce-scattered back; the collectives are in section
+    "NVLink-Based Cross-GPU Collaboration").  Read as: each rank scores its own items' rows against every
+    gathered column, so the shares of bands that partition the rows add up to the whole.
     """
     e = _f64(e)
     n = e.shape[0]

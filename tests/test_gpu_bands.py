@@ -1,9 +1,10 @@
 """Anchor bands of the pooled loss on the GPU, against the float64 oracle.
 
-A band is one device's rows when the loss is sharded by rows ("UForm", section "NVLink-Based Cross-GPU
-Collaboration": each device scores its band of anchor rows against every column, and the gradients are
-reduce-scattered).  Run on one GPU: each band's results are the oracle's band shares, and bands that
-partition the rows add up to the whole call.
+A band is one device's rows when the loss is sharded across devices ("UForm", section "Matryoshka-Like
+Multi-Scale Embedders": the per-rank embeddings all-gathered into one similarity band, the gradients
+reduce-scattered back), read as each rank scoring its own items' rows against every gathered column.
+Run on one GPU: each band's results are the oracle's band shares, and bands that partition the rows add
+up to the whole call.
 """
 
 import numpy as np

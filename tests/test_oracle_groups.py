@@ -113,8 +113,9 @@ def test_finite_differences():
 
 
 # ---------------------------------------------------------------------------
-# Anchor bands: one device's rows when the loss is sharded by rows ("UForm", section "NVLink-Based
-# Cross-GPU Collaboration": each device scores its band of rows against every column).
+# Anchor bands: one device's rows when the loss is sharded across devices ("UForm", section
+# "Matryoshka-Like Multi-Scale Embedders": embeddings all-gathered into one similarity band, gradients
+# reduce-scattered back), read as each rank scoring its own items' rows against every gathered column.
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("named", [False, True])
