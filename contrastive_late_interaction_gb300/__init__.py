@@ -14,7 +14,7 @@ _BINDING_NAMES = {
     "raise_for", "pair_loss_scores_fwd_bwd", "pair_loss_scores_workspace_bytes",
     "pair_loss_sigmoid_matryoshka_fwd_bwd", "pair_loss_sigmoid_matryoshka_workspace_bytes",
     "pair_loss_sigmoid_groups_fwd_bwd", "maxsim_scores_named", "maxsim_named_workspace_bytes",
-    "maxsim_backward_named",
+    "maxsim_backward_named", "selftest_bounded_wait",
 }
 
 

@@ -158,6 +158,7 @@ EXPORTS = {
     "maxsim_backward_named": (c_int, [ctypes.POINTER(MaxSimBackwardNamedArgs)]),
     "maxsim_backward_workspace_bytes": (c_size_t, [c_size_t, c_size_t, c_size_t, c_size_t, c_size_t]),
     "maxsim_backward_no_alloc": (c_int, [ctypes.POINTER(MaxSimBackwardArgs)]),
+    "cli_selftest_bounded_wait": (c_int, [c_void_p, c_void_p, ctypes.c_uint32, c_void_p]),
 }
 NO_ALLOC_MAX_QUERY_ROWS = 262144   # CLI_MAXSIM_NO_ALLOC_MAX_QUERY_ROWS in include/cli.h
 
@@ -245,6 +246,20 @@ def _band(band):
 
 def _ws(nbytes, device):
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def selftest_bounded_wait(limit_us=20000, device_status=None, gave_up=None, stream=None):
+    """Runs the failure path of the kernels' bounded waits (one CTA waiting on a barrier nothing arrives
+    at, giving up after `limit_us`).  Returns dict(device_status, gave_up) of device int32 tensors; the
+    status reads CLI_INTERNAL and gave_up the number of threads (64) once the stream reaches them."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = device_status if device_status is not None else torch.zeros(1, dtype=torch.int32, device=dev)
+    gu = gave_up if gave_up is not None else torch.zeros(1, dtype=torch.int32, device=dev)
+    _check_cuda(st, "device_status", torch.int32)
+    _check_cuda(gu, "gave_up", torch.int32)
+    raise_for(lib.cli_selftest_bounded_wait(_ptr(st), _ptr(gu), int(limit_us), _stream(stream)),
+              "cli_selftest_bounded_wait")
+    return dict(device_status=st, gave_up=gu)
 
 
 def check_device_status(status: torch.Tensor, where: str = "device"):

@@ -90,14 +90,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 // Every wait in these kernels is bounded: after kWaitLimitNs of no progress the
 // waiter raises the CTA's abort flag (and reports CLI_INTERNAL); every other
-// waiter of the CTA sees the flag and gives up too, so the kernel returns.
+// waiter of the CTA sees the flag and gives up too, so the kernel returns.  A
+// cap on the number of probes backs up the clock: no wait of these kernels
+// comes near it (they last microseconds), and it ends the loop even if the
+// global timer did not advance.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint32_t kWaitProbeLimit = 1u << 24;
 
 // `sleep_ns` > 0 puts the thread to sleep that long between failed probes, so a
 // waiter whose wake-up is not on the critical path (a TMA producer, say) leaves
-// the issue slots to the warps doing the work.
+// the issue slots to the warps doing the work.  `limit_ns` shortens the bound
+// (the failure-detection self-test uses it).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *status, uint32_t sleep_ns = 0) {
+                                          int32_t *status, uint32_t sleep_ns = 0,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t spin = 1;; ++spin) {
@@ -106,7 +112,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
         if (spin < 4096 ? mbar_try_wait(bar, parity) : mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if ((spin & 255u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit_ns || spin >= kWaitProbeLimit) {
                 *abort_flag = 1;
                 report(status, CLI_INTERNAL);
                 return false;

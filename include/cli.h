@@ -440,6 +440,24 @@ cli_status_t maxsim_backward_named(const cli_maxsim_backward_named_t *args);
 #define CLI_MAXSIM_NO_ALLOC_MAX_QUERY_ROWS 262144
 cli_status_t maxsim_backward_no_alloc(const cli_maxsim_backward_t *args);
 
+/*
+ * cli_selftest_bounded_wait -- runs the failure path of the kernels' bounded
+ * waits, faulting nothing.  Every wait of the tensor-core kernels gives up
+ * after a time limit (2 s in the verbs above): the waiter writes CLI_INTERNAL
+ * to the device status and raises its CTA's abort flag, the CTA's other
+ * waiters give up too, and the kernel returns with the context usable.  This
+ * call enqueues one CTA of 64 threads that wait on an mbarrier nothing arrives
+ * at, with a limit of `limit_us` microseconds.
+ *
+ *   device_status   device int32 (written: CLI_INTERNAL once the wait gives up)
+ *   gave_up         device int32, or NULL (written: the number of threads
+ *                   whose wait gave up, 64)
+ *   limit_us        1 .. 2,000,000; anything else is CLI_INVALID_ARGUMENT, as
+ *                   is a NULL device_status
+ *   stream          cudaStream_t
+ */
+cli_status_t cli_selftest_bounded_wait(int32_t *device_status, int32_t *gave_up, uint32_t limit_us, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -36,6 +36,13 @@ def test_every_declared_symbol_is_exported(b):
     assert names == set(b.EXPORTS)
 
 
+def test_selftest_host_checks(b):
+    f = b.lib.cli_selftest_bounded_wait
+    assert f(None, None, 1000, None) == b.CLI_INVALID_ARGUMENT
+    assert f(A * 1, None, 0, None) == b.CLI_INVALID_ARGUMENT
+    assert f(A * 1, A * 2, 2000001, None) == b.CLI_INVALID_ARGUMENT
+
+
 def test_status_names(b):
     assert [b.status_name(i) for i in range(7)] == b.STATUS_NAMES
     assert b.status_name(99) == "unknown"
