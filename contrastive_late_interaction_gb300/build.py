@@ -62,20 +62,25 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
         return obj, r.stdout + r.stderr
 
-    with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        results = list(ex.map(compile_one, srcs))
-    if verbose or ptxas_info:
-        for _, log in results:
-            if log.strip():
-                sys.stderr.write(log)
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *[o for o, _ in results]]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    for o, _ in results:
-        os.remove(o)
-    if r.returncode != 0:
-        raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    try:
+        with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
+            results = list(ex.map(compile_one, srcs))
+        if verbose or ptxas_info:
+            for _, log in results:
+                if log.strip():
+                    sys.stderr.write(log)
+        tmp = LIB + f".tmp{os.getpid()}"
+        cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *[o for o, _ in results]]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, LIB)
+    finally:
+        # this build's objects, whether or not every unit compiled
+        for src in srcs:
+            obj = os.path.join(BUILD, os.path.basename(src) + f".{os.getpid()}.o")
+            if os.path.exists(obj):
+                os.remove(obj)
     return LIB
 
 
