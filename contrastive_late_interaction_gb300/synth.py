@@ -52,14 +52,19 @@ STREAM_GROUPS = 12
 STREAM_NAMED = 13
 
 
+# Shift counts as one-element arrays: some numpy releases take a slow path for a uint64 array shifted by a
+# uint64 scalar (the values are the same either way).
+_S11, _S27, _S30, _S31 = (np.full(1, k, dtype=np.uint64) for k in (11, 27, 30, 31))
+
+
 def _mix(z: np.ndarray) -> np.ndarray:
     z = np.asarray(z, dtype=np.uint64)
     with np.errstate(over="ignore"):
-        z = z ^ (z >> np.uint64(30))
+        z = z ^ (z >> _S30)
         z = z * _M1
-        z = z ^ (z >> np.uint64(27))
+        z = z ^ (z >> _S27)
         z = z * _M2
-        z = z ^ (z >> np.uint64(31))
+        z = z ^ (z >> _S31)
     return z
 
 
@@ -80,13 +85,13 @@ def words(seed: int, stream: int, start: int, count: int) -> np.ndarray:
 def uniform_open0(seed: int, stream: int, start: int, count: int) -> np.ndarray:
     """Uniforms on (0, 1]."""
     w = words(seed, stream, start, count)
-    return ((w >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0**-53
+    return ((w >> _S11).astype(np.float64) + 1.0) * 2.0**-53
 
 
 def uniform_closed0(seed: int, stream: int, start: int, count: int) -> np.ndarray:
     """Uniforms on [0, 1)."""
     w = words(seed, stream, start, count)
-    return (w >> np.uint64(11)).astype(np.float64) * 2.0**-53
+    return (w >> _S11).astype(np.float64) * 2.0**-53
 
 
 def normal(seed: int, stream: int, start: int, count: int) -> np.ndarray:
@@ -366,3 +371,66 @@ def named_documents(seed: int, nq: int, nd: int, others: int) -> tuple[Edges, Ed
         att.append([own])
         rep.append(sorted(picked))
     return edges_from_lists(att), edges_from_lists(rep)
+
+
+def maxsim_ties(seed: int, regime: str, nq: int = 24, nd: int = 60, width: int = 64,
+                q_len: tuple[int, int] = (1, 70), d_len: tuple[int, int] = (1, 300)) -> MaxSimInputs:
+    """MaxSim inputs whose every (query row, document) maximum is an exact tie between identical rows.
+
+    Every query row points along feature 0: q = 0.99 e0 + 0.14 n with n a unit vector on features
+    1 .. width/2 - 1.  Each document holds one "winner" row W repeated at 2..5 positions (every row, for
+    one document in seven; adjacent documents share W in pairs), the rest "background" rows:
+      regime "positive": W = 0.5 e0 + ..., background e0-components in [-0.5, 0.1], so the maximum is
+                          the winner, between 0.37 and 0.64;
+      regime "negative": W = -0.15 e0 + ..., background in [-0.9, -0.5]: every score is negative and the
+                          winner, between -0.29 and -0.01, is the maximum;
+      regime "zero":     W is zero on features 0 .. width/2 - 1 (orthogonal to every query row, so its
+                          score is exactly zero) and the background is as in "negative".
+    The remaining components of each row are a unit vector on the other features, scaled to make the row
+    unit.  Identical rows give bit-identical scores on both sides, so the maximum is reached at every
+    winner position and the argmax is the lowest one."""
+    half = width // 2
+    ql = uniform_int(seed, STREAM_QUERY_LENGTHS, nq, *q_len)
+    dl = uniform_int(seed, STREAM_DOC_LENGTHS, nd, *d_len)
+    qo, do = ragged_offsets(ql), ragged_offsets(dl)
+    rows_q, rows_d = int(qo[-1]), int(do[-1])
+    n = normal(seed, STREAM_QUERY_ROWS, 0, rows_q * (half - 1)).reshape(rows_q, half - 1)
+    n /= np.linalg.norm(n, axis=1, keepdims=True)
+    q = np.zeros((rows_q, width))
+    q[:, 0] = 0.99
+    q[:, 1:half] = 0.14 * n
+    u = uniform_closed0(seed, STREAM_DOC_ROWS, 0, rows_d + 8 * nd)
+    g = normal(seed, STREAM_DOC_ROWS, rows_d + 8 * nd, (rows_d + nd) * width).reshape(rows_d + nd, width)
+
+    def row(sigma, k, zero_half=False):
+        v = g[k].copy()
+        v[0] = 0.0
+        if zero_half:
+            v[:half] = 0.0
+        v /= np.linalg.norm(v)
+        r = np.sqrt(1.0 - sigma * sigma) * v
+        r[0] = sigma
+        return r
+
+    w_sigma = {"positive": 0.5, "negative": -0.15, "zero": 0.0}[regime]
+    bg_lo, bg_hi = (-0.5, 0.1) if regime == "positive" else (-0.9, -0.5)
+    d = np.zeros((rows_d, width))
+    winners = [row(w_sigma, rows_d + (i // 2), zero_half=regime == "zero") for i in range(nd)]
+    for i in range(nd):
+        r0, r1 = int(do[i]), int(do[i + 1])
+        length = r1 - r0
+        for s in range(length):
+            d[r0 + s] = row(bg_lo + (bg_hi - bg_lo) * u[r0 + s], r0 + s)
+        if i % 7 == 3:
+            pos = np.arange(length)
+        else:
+            k = min(length, 2 + int(u[rows_d + 8 * i] * 4))
+            pick = np.floor(u[rows_d + 8 * i + 1:rows_d + 8 * i + 1 + 2 * k] * length).astype(np.int64)
+            pos = np.unique(pick)[:k]
+            if length > 1 and pos.size < 2:
+                pos = np.array([0, length - 1])
+        d[r0 + pos] = winners[i]
+    qb = bf16_bits(q.astype(np.float32))
+    db = bf16_bits(d.astype(np.float32))
+    ds = normal(seed, STREAM_D_SCORES, 0, nq * nd).reshape(nq, nd).astype(np.float32)
+    return MaxSimInputs(width, qo, qb, do, db, ds)
