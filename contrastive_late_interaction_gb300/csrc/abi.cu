@@ -495,9 +495,19 @@ int chunk_rows_for(size_t rows_d, size_t rows_q, int sms) {
 struct MaxSimWs {
     float *mval;
     uint32_t *chunk_doc;
+    unsigned long long *fix_list;
+    uint32_t *fix_count;
+    uint32_t fix_cap;
     size_t bytes;
     int n_chunks, chunk_rows;
 };
+
+// Argmax entries the forward lists for the float64 fix-up (rows whose maximum
+// over a document is <= 0 or subnormal); past this many it scans its whole table.
+size_t fix_capacity(size_t nd, size_t rows_q) {
+    const size_t all = nd * rows_q;
+    return all < (size_t{1} << 18) ? all : (size_t{1} << 18);
+}
 
 // Named pairs run on the finest chunks (1024 document rows), so that items
 // holding no named pair are skipped at a fine grain.
@@ -513,6 +523,11 @@ MaxSimWs carve_maxsim(void *base, size_t nd, size_t rows_q, size_t rows_d, int s
     w.n_chunks = static_cast<int>((rows_d + w.chunk_rows - 1) / w.chunk_rows);
     w.chunk_doc = reinterpret_cast<uint32_t *>(p ? p + off : nullptr);
     off += align256((static_cast<size_t>(w.n_chunks) + 1) * sizeof(uint32_t));
+    w.fix_cap = static_cast<uint32_t>(fix_capacity(nd, rows_q));
+    w.fix_list = reinterpret_cast<unsigned long long *>(p ? p + off : nullptr);
+    off += align256(static_cast<size_t>(w.fix_cap) * sizeof(unsigned long long));
+    w.fix_count = reinterpret_cast<uint32_t *>(p ? p + off : nullptr);
+    off += align256(2 * sizeof(uint32_t));
     w.bytes = off;
     return w;
 }
@@ -525,7 +540,9 @@ size_t maxsim_workspace_bytes(size_t query_count, size_t document_count, size_t 
     (void)width;
     // The chunking depends on the SM count; size for the smallest chunks (most chunks).
     const size_t chunks = (document_rows + 1023) / 1024 + 1;
-    return align256(document_count * query_rows * sizeof(float)) + align256((chunks + 1) * sizeof(uint32_t));
+    return align256(document_count * query_rows * sizeof(float)) + align256((chunks + 1) * sizeof(uint32_t)) +
+           align256(fix_capacity(document_count, query_rows) * sizeof(unsigned long long)) +
+           align256(2 * sizeof(uint32_t));
 }
 
 }  // extern "C"
@@ -594,6 +611,11 @@ cli_status_t maxsim_forward_call(const cli_maxsim_t *a, const cli_edges_t *pairs
     L.chunk_doc = ws.chunk_doc;
     L.n_chunks = ws.n_chunks;
     L.chunk_rows = ws.chunk_rows;
+    L.q = static_cast<const uint16_t *>(a->queries.data);
+    L.d = static_cast<const uint16_t *>(a->documents.data);
+    L.fix_list = ws.fix_list;
+    L.fix_count = ws.fix_count;
+    L.fix_cap = ws.fix_cap;
     L.status = a->device_status;
     L.sm_count = sms;
     if (pairs) {

@@ -137,6 +137,12 @@ struct MaxSimLaunch {
     uint32_t *item_flags = nullptr;   // [n_chunks * n_mblocks]
     uint32_t *item_list = nullptr;    // [n_chunks * n_mblocks]
     uint32_t *item_count = nullptr;   // [1]
+    // The tapes (bf16 rows) for the float64 argmax fix-up, and its workspace: the
+    // listed entries (document << 32 | row), [count, overflow flag], capacity.
+    const uint16_t *q = nullptr, *d = nullptr;
+    unsigned long long *fix_list = nullptr;
+    uint32_t *fix_count = nullptr;
+    uint32_t fix_cap = 0;
 };
 cudaError_t launch_maxsim_forward(const CUtensorMap &tmap_q, const CUtensorMap &tmap_d, const MaxSimLaunch &L,
                                   cudaStream_t stream);

@@ -13,12 +13,17 @@
 // row across the tiles of the current document; the boundaries between
 // documents are the same for every row, so the segment logic is warp-uniform.
 // Per 32-column chunk each score becomes a key that carries the column in the
-// 5 low mantissa bits (31 - column, so equal values resolve to the lowest
-// column; one ALU instruction per cell).  For a chunk inside one document the
-// keys go back into TMEM and a reducing TMEM load returns their maximum; a
-// chunk holding a document boundary masks its keys per segment and reduces
-// them with a tree of three-input max operations.  The reported value is
-// truncated by less than 2^-18 relative.
+// 5 low mantissa bits (31 - column, so among equal positive values the largest
+// key names the lowest column; one ALU instruction per cell).  For a chunk
+// inside one document the keys go back into TMEM and a reducing TMEM load
+// returns their maximum; a chunk holding a document boundary masks its keys per
+// segment and reduces them with a tree of three-input max operations.  The
+// reported value is truncated by less than 2^-18 relative.  A row whose
+// maximum over a document is not a positive normal number (every score of the
+// document negative, whose keys order equal values the other way, or zero, or
+// subnormal) is listed by the per-query sums, which read every maximum anyway,
+// and `argmax_fixup_kernel` finds its argmax again in float64 from the tapes,
+// the lowest row among equal scores; the tile kernel does nothing for it.
 //
 // The ragged schedule: the document tape is cut into chunks of whole
 // documents of about `chunk_rows` rows (a binary search over the offsets per
@@ -85,8 +90,14 @@ __device__ __forceinline__ void item_at(const Params &P, long long w, int &chunk
 // Keys: each score's bits with the 5 low mantissa bits replaced by 31 - column
 // (one lop3, the mask ~31 held in a register so the two-constant form does not
 // split into two operations).  The largest key is the largest score truncated
-// by less than 2^-18 relative, and among equal truncated scores it names the
-// lowest column.
+// by less than 2^-18 relative.  Among equal truncated scores that are positive
+// it names the lowest column.  Among negative ones a larger low field makes a
+// smaller float, so it names the highest column, and a zero or subnormal
+// maximum may be flushed by a reducing load: a key that is not a positive
+// normal number does not decode to the lowest column.  A document maximum that
+// is a positive normal number came from a key that does (truncation keeps a
+// positive normal value positive and normal), so a row whose maximum over the
+// document is anything else goes to the float64 fix-up.
 
 // Running (max, argmax) update from the largest key of a chunk's columns of the
 // current document; `base` is the chunk's first row relative to the document.
@@ -474,22 +485,6 @@ __global__ void __launch_bounds__(kCompactThreads) compact_items_kernel(const F 
     if (threadIdx.x == kCompactThreads - 1) *count = part[threadIdx.x];
 }
 
-// S(q, d) = 0 for every pair no query names (one thread per cell).
-__global__ void mask_scores_kernel(const uint64_t *pair_off, const uint32_t *pair_ids, int nq, int nd, float *scores,
-                                   long long ld_scores, const int32_t *status) {
-    if (read_status(status) != 0) return;
-    const long long cell = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (cell >= static_cast<long long>(nq) * nd) return;
-    const int q = static_cast<int>(cell / nd), d = static_cast<int>(cell % nd);
-    uint64_t lo = pair_off[q], hi = pair_off[q + 1];
-    while (lo < hi) {
-        const uint64_t mid = (lo + hi) >> 1;
-        if (pair_ids[mid] < static_cast<uint32_t>(d)) lo = mid + 1; else hi = mid;
-    }
-    const bool named = lo < pair_off[q + 1] && pair_ids[lo] == static_cast<uint32_t>(d);
-    if (!named) scores[static_cast<long long>(q) * ld_scores + d] = 0.0f;
-}
-
 // chunk_doc[k] = first document starting at or after row k * chunk_rows;
 // chunk_doc[n_chunks] = nd.
 __global__ void schedule_kernel(const uint64_t *d_off, int nd, int n_chunks, long long chunk_rows,
@@ -511,19 +506,130 @@ __global__ void schedule_kernel(const uint64_t *d_off, int nd, int n_chunks, lon
 }
 
 // S[q][d] = sum over the query's rows of m[d][t], in row order (/ |q| if mean).
+// A maximum that is not a positive normal number (its argmax came from a key
+// that need not name the lowest row) is listed for `argmax_fixup_kernel`:
+// (document << 32 | row) in list[0 .. cap), count[0] the number found, count[1]
+// set when they do not fit.  With named pairs (pair_off not null) a pair no
+// query names scores 0 and lists nothing (its items may not have run).
 __global__ void query_sum_kernel(const float *mval, const uint64_t *q_off, int nq, int nd, int rows_q, int mean,
-                                 float *scores, long long ld, const int32_t *status) {
+                                 float *scores, long long ld, unsigned long long *list, uint32_t *count, uint32_t cap,
+                                 const uint64_t *pair_off, const uint32_t *pair_ids, const int32_t *status) {
     if (read_status(status) != 0) return;
     const long long total = static_cast<long long>(nq) * nd;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int d = static_cast<int>(idx / nq), q = static_cast<int>(idx % nq);
+        if (pair_off) {
+            uint64_t lo = pair_off[q], hi = pair_off[q + 1];
+            while (lo < hi) {
+                const uint64_t mid = (lo + hi) >> 1;
+                if (pair_ids[mid] < static_cast<uint32_t>(d)) lo = mid + 1; else hi = mid;
+            }
+            if (!(lo < pair_off[q + 1] && pair_ids[lo] == static_cast<uint32_t>(d))) {
+                scores[static_cast<long long>(q) * ld + d] = 0.0f;
+                continue;
+            }
+        }
         const uint64_t a = q_off[q], b = q_off[q + 1];
         const float *m = mval + static_cast<long long>(d) * rows_q;
-        float s = 0.f;
-        for (uint64_t t = a; t < b; ++t) s += m[t];
+        float s = 0.f, lowest = INFINITY;
+        for (uint64_t t = a; t < b; ++t) {
+            const float v = m[t];
+            s += v;
+            lowest = fminf(lowest, v);
+        }
+        if (!(lowest >= 1.17549435e-38f)) {   // rare: some row's scores all <= 0 over the document, or subnormal
+            for (uint64_t t = a; t < b; ++t) {
+                if (m[t] >= 1.17549435e-38f) continue;
+                const uint32_t k = atomicAdd(count, 1u);
+                if (k < cap)
+                    list[k] = (static_cast<unsigned long long>(d) << 32) | static_cast<uint32_t>(t);
+                else
+                    atomicOr(count + 1, 1u);
+            }
+        }
         if (mean) s /= static_cast<float>(b - a);
         scores[static_cast<long long>(q) * ld + d] = s;
+    }
+}
+
+// The argmax entries whose row maximum over the document is not a positive
+// normal number (every score of the document <= 0 for that row, or a subnormal
+// maximum): their key's column need not be the lowest among equal scores.  One
+// warp per entry finds the argmax again from the tapes: every document row's
+// score in float64 (each bf16 product is exact in float64, and so, far below any
+// difference a float32 score could show, is their sum), keeping the lowest row
+// among equal scores, and writes it.  The warps take the entries the per-query
+// sums listed; after an overflow of the list they scan the maxima for such
+// entries instead.
+struct FixupArgs {
+    const uint16_t *q, *d;
+    const uint64_t *d_off;
+    int width, nd, rows_q;
+    int32_t *argmax;
+    long long ld_argmax;
+    const float *mval;
+    const unsigned long long *list;
+    const uint32_t *count;   // [0] entries found, [1] overflow flag
+    uint32_t cap;
+    const int32_t *status;
+};
+
+__device__ __forceinline__ double bf16_to_f64(uint16_t b) {
+    return static_cast<double>(__uint_as_float(static_cast<uint32_t>(b) << 16));
+}
+
+__device__ void fix_entry(const FixupArgs &A, int d, int t, int lane) {
+    const long long r0 = static_cast<long long>(A.d_off[d]);
+    const long long len = static_cast<long long>(A.d_off[d + 1]) - r0;
+    const uint16_t *qr = A.q + static_cast<long long>(t) * A.width;
+    double bv = -INFINITY;
+    long long bi = 0;
+    for (long long s = lane; s < len; s += 32) {   // ascending: a strict comparison keeps the lowest row
+        const uint16_t *dr = A.d + (r0 + s) * A.width;
+        double acc = 0.0;
+        for (int k = 0; k < A.width; ++k) acc += bf16_to_f64(qr[k]) * bf16_to_f64(dr[k]);
+        if (acc > bv) {
+            bv = acc;
+            bi = s;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const long long oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) {
+            bv = ov;
+            bi = oi;
+        }
+    }
+    if (lane == 0) A.argmax[static_cast<long long>(d) * A.ld_argmax + t] = static_cast<int32_t>(bi);
+}
+
+__global__ void __launch_bounds__(256) argmax_fixup_kernel(FixupArgs A) {
+    if (read_status(A.status) != 0) return;
+    const int lane = threadIdx.x & 31;
+    const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const long long warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    if (A.count[1] == 0) {
+        const long long n = min(static_cast<long long>(A.count[0]), static_cast<long long>(A.cap));
+        for (long long e = warp; e < n; e += warps) {
+            const unsigned long long v = A.list[e];
+            fix_entry(A, static_cast<int>(v >> 32), static_cast<int>(v & 0xFFFFFFFFu), lane);
+        }
+        return;
+    }
+    const long long total = static_cast<long long>(A.nd) * A.rows_q;
+    for (long long b = warp * 32; b < total; b += warps * 32) {   // warp-uniform trip count
+        const long long i = b + lane;
+        const int d = static_cast<int>(i / A.rows_q), t = static_cast<int>(i % A.rows_q);
+        const bool marked = i < total && !(A.mval[i] >= 1.17549435e-38f);
+        unsigned m = __ballot_sync(0xffffffffu, marked);
+        while (m) {
+            const int l = __ffs(m) - 1;
+            m &= m - 1;
+            fix_entry(A, __shfl_sync(0xffffffffu, d, l), __shfl_sync(0xffffffffu, t, l), lane);
+        }
     }
 }
 
@@ -1019,6 +1125,7 @@ cudaError_t launch_maxsim_forward(const CUtensorMap &tmap_q, const CUtensorMap &
     P.status = L.status;
     P.item_list = nullptr;
     P.item_count = nullptr;
+    if ((err = cudaMemsetAsync(L.fix_count, 0, 2 * sizeof(uint32_t), stream)) != cudaSuccess) return err;
     if (L.pair_off) {   // named pairs: run only the items that hold one
         const long long n_items = P.items;
         if ((err = cudaMemsetAsync(L.item_flags, 0, static_cast<size_t>(n_items) * 4, stream)) != cudaSuccess) return err;
@@ -1047,14 +1154,26 @@ cudaError_t launch_maxsim_forward(const CUtensorMap &tmap_q, const CUtensorMap &
     forward_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmap_q, tmap_d, P);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     query_sum_kernel<<<L.sm_count * 8, 256, 0, stream>>>(L.mval, L.q_off, L.nq, L.nd, L.rows_q, L.mean, L.scores,
-                                                          L.ld_scores, L.status);
+                                                          L.ld_scores, L.fix_list, L.fix_count, L.fix_cap, L.pair_off,
+                                                          L.pair_ids, L.status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    if (L.pair_off) {
-        const long long cells = static_cast<long long>(L.nq) * L.nd;
-        mask_scores_kernel<<<static_cast<unsigned>((cells + 255) / 256), 256, 0, stream>>>(
-            L.pair_off, L.pair_ids, L.nq, L.nd, L.scores, L.ld_scores, L.status);
-    }
-    return cudaGetLastError();
+    FixupArgs F;
+    F.q = L.q;
+    F.d = L.d;
+    F.d_off = L.d_off;
+    F.width = L.width;
+    F.nd = L.nd;
+    F.rows_q = L.rows_q;
+    F.argmax = L.argmax;
+    F.ld_argmax = L.ld_argmax;
+    F.mval = L.mval;
+    F.list = L.fix_list;
+    F.count = L.fix_count;
+    F.cap = L.fix_cap;
+    F.status = L.status;
+    argmax_fixup_kernel<<<L.sm_count * 2, 256, 0, stream>>>(F);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    return cudaSuccess;
 }
 
 cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream) {

@@ -310,7 +310,13 @@ typedef struct {
  *     S(q, d) = sum_{t in q} max_{s in d} <q_t, d_s>       (mean = 0)
  *     S(q, d) = (1/|q|) sum_{t in q} max_{s in d} <q_t, d_s>  (mean = 1)
  * plus the argmax, the document-local index of the best row, lowest index on
- * ties, for every query token and document.
+ * ties, for every query token and document ("UForm", section "ColBERT-Style
+ * Late-Interaction Rerankers": each query token keeps its single best match).
+ * Scores are compared in float32 with the low 5 mantissa bits dropped (under
+ * 2^-18 relative), so scores closer than that count as tied; where a token's
+ * best score over a document is not a positive normal number (every score of
+ * the document <= 0 for that token, or subnormal) the argmax is found again
+ * in float64 from the tapes, again the lowest index among equal scores.
  *
  *   width     token width D, a multiple of 8, at most 256 (the pages: a
  *             multiple of 8, 128 by default)
@@ -343,8 +349,10 @@ size_t maxsim_workspace_bytes(size_t query_count, size_t document_count, size_t 
  * score the documents it attracts and repels, a document is scored by the
  * queries naming it).  S(q, d) and the argmax of every named pair are those of
  * maxsim_scores; for a pair no query names, S(q, d) = 0 and its argmax
- * entries are row indices of the document (0 where its work item was skipped),
- * so maxsim_backward runs on the same outputs (with dS = 0 there, as the
+ * entries are row indices of the document (0 where its work item was skipped;
+ * after more than 2^18 float64 argmax recomputations in one call, possibly the
+ * true argmax row instead), so maxsim_backward runs on the same outputs (with
+ * dS = 0 there, as the
  * named-negatives loss over S gives).  Work items (1024 document rows by 128
  * query rows) that hold no named pair are not computed.
  *
@@ -433,9 +441,10 @@ cli_status_t maxsim_backward_named(const cli_maxsim_backward_named_t *args);
  * loading the library holds until the process exits.  A query tape of more
  * rows returns CLI_UNSUPPORTED.  Every call shares that array: calls whose
  * kernels overlap on the GPU (other streams or host threads) race on it.  The
- * first call on each device looks the array's address up and caches it; make
- * that call before any stream capture.  Nothing here calls cudaMalloc, cudaFree
- * or any allocating routine.
+ * first call on each device looks the array's address up and caches it with
+ * the device's current context; make that call before any stream capture.  A
+ * call in another context (after cudaDeviceReset) looks it up again.  Nothing
+ * here calls cudaMalloc, cudaFree or any allocating routine.
  */
 #define CLI_MAXSIM_NO_ALLOC_MAX_QUERY_ROWS 262144
 cli_status_t maxsim_backward_no_alloc(const cli_maxsim_backward_t *args);
