@@ -15,9 +15,13 @@
 // before reading it, so nothing needs clearing, but two calls whose kernels
 // overlap on the GPU (different streams, or different host threads) race on
 // it.  The first call on each device looks the array's device address up (with
-// that device current) and caches it; make that first call before any stream
-// capture.
+// that device current) and caches it with the device's current context; make
+// that first call before any stream capture.  After cudaDeviceReset the
+// context, and with it the array's address, changes: a call in the new
+// context looks the address up again.
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -33,21 +37,44 @@ constexpr size_t kNoAllocMaxQueryRows = CLI_MAXSIM_NO_ALLOC_MAX_QUERY_ROWS;
 static __device__ __align__(256) int32_t g_query_of_row[kNoAllocMaxQueryRows];
 
 constexpr int kMaxDevices = 64;
-int32_t *g_scratch_ptr[kMaxDevices] = {};
+struct Scratch {
+    int32_t *ptr;
+    CUcontext ctx;   // the context the address belongs to
+};
+Scratch g_scratch[kMaxDevices] = {};
 std::mutex g_scratch_mutex;
 
-// Device address of g_query_of_row on the current device (looked up once per
-// device); NULL on failure.
+// The calling thread's current context (NULL before the runtime has made one
+// current), through the driver entry point, so the library needs no libcuda link.
+CUcontext current_context() {
+    static PFN_cuCtxGetCurrent_v4000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        return cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+                       q == cudaDriverEntryPointSuccess
+                   ? reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p)
+                   : nullptr;
+    }();
+    CUcontext ctx = nullptr;
+    if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+    return ctx;
+}
+
+// Device address of g_query_of_row on the current device, looked up once per
+// device and context; NULL on failure.
 int32_t *scratch_for_current_device() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    CUcontext ctx = current_context();
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[dev]) {
+    Scratch &s = g_scratch[dev];
+    if (!s.ptr || !ctx || ctx != s.ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_query_of_row) != cudaSuccess || !p) return nullptr;
-        g_scratch_ptr[dev] = static_cast<int32_t *>(p);
+        s.ptr = static_cast<int32_t *>(p);
+        s.ctx = current_context();   // current now that the runtime has set the device up
     }
-    return g_scratch_ptr[dev];
+    return s.ptr;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
