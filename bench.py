@@ -46,6 +46,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work budget of the oracle baseline")
+    ap.add_argument("--no-extra-parts", action="store_true",
+                    help="with the joint workload, skip the separately timed config-4 pooled and config-3 MaxSim calls")
     return ap.parse_args()
 
 
@@ -262,12 +264,12 @@ class Step:
             else:
                 n += 3                                    # fused block kernel, two-level final reduction
         if self.m is not None:
-            n += 2 + 1 + 1 + 1                            # 2 tape validations, schedule, forward, query sums
+            n += 2 + 1 + 1 + 1 + 1                        # 2 tape validations, schedule, forward, query sums, fix-up
             if not self.named:
                 n += 2 + 1 + 1 + 1                        # 2 tape validations, row->query map, dQ, dD
             if self.named:
                 n += 2 + 1 + 1                            # 2 tape validations, pair validation, named backward
-                n += 1 + 1 + 1 + 1                        # pair validation, item marks, compaction, score mask
+                n += 1 + 1 + 1                            # pair validation, item marks, compaction
                 n += 2 + 1 + 1                            # 2 edge validations, score loss, final reduction
             if self.j is not None:
                 n += 1 + 1 + 1                            # edge validation, score loss, final reduction
@@ -338,12 +340,29 @@ class Step:
         return sum(h.numel() * h.element_size() for h in self.host.values())
 
     def results(self):
+        """The step's results a caller reads back: the losses and their scalar gradients, dE, the MaxSim
+        score matrix, dQ and dD (the argmax and dS are intermediates the backward consumes on the device)."""
         outs = []
         if self.p is not None:
-            outs += [self.p_out["loss"], self.p_out["d_inverse_temperature"], self.p_out["d_bias"]]
+            outs += [self.p_out["loss"], self.p_out["d_inverse_temperature"], self.p_out["d_bias"],
+                     self.p_out["d_embeddings"]]
+        if self.m is not None:
+            outs += [self.f_out["scores"], self.b_out["d_queries"], self.b_out["d_documents"]]
         if self.j is not None or self.named:
             outs += [self.s_out["loss"], self.s_out["d_inverse_temperature"], self.s_out["d_bias"]]
         return outs
+
+    def active_pairs(self):
+        """(query row, document) pairs whose c = dS[q, d] is nonzero, read from the step's dS on the device
+        (every pair without a score loss and with the random dS)."""
+        m = self.m
+        if self.j is not None or self.named:
+            ds = self.s_out["d_scores"]
+        else:
+            ds = self.ds
+        nz = (ds != 0).sum(dim=1).double().cpu().numpy()
+        ql = np.diff(m.q_offsets.astype(np.int64)).astype(np.float64)
+        return float(np.sum(nz * ql))
 
     def statuses(self):
         st = []
@@ -617,6 +636,106 @@ def run_reference(args, world, rank):
     return 0
 
 
+def step_names(step):
+    """The per-call event names of a step, in launch order."""
+    names = []
+    if step.p is not None:
+        names.append("pooled")
+    if step.m is not None:
+        names.append("maxsim_fwd")
+        if step.j is not None or step.named is not None:
+            names.append("score_loss")
+        names.append("maxsim_bwd")
+    return names
+
+
+def timed_region(step, stream, flush, steps, device_index, pg=None):
+    """K steps on the step's stream, the L2 flushed between them (outside the per-step events), bracketed by a
+    barrier and a device synchronisation on both sides, with nvidia-smi clocks sampled inside.  Returns
+    (per-step ms, {call: per-step ms}, clock summary, wall seconds)."""
+    import torch
+    names = step_names(step)
+    ev = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for n in names}
+          for _ in range(steps)]
+    st_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(device_index) as clocks:
+        clocks.mark(True)
+        wall0 = time.perf_counter()
+        for k in range(steps):
+            with torch.cuda.stream(stream):
+                flush.fill_(k & 0xFF)
+                st_ev[k][0].record(stream)
+                step.run(ev[k])
+                st_ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        clocks.mark(False)
+    if pg is not None:
+        pg.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in st_ev]
+    part_ms = {n: [ev[k][n][0].elapsed_time(ev[k][n][1]) for k in range(steps)] for n in names}
+    return step_ms, part_ms, clocks.summary(), wall
+
+
+def warm(step, stream, warmup):
+    for _ in range(max(3, warmup)):
+        step.run()
+    stream.synchronize()
+    bad = [s for s in step.statuses() if s != 0]
+    if bad:
+        raise SystemExit(f"device status {bad} after warm-up")
+
+
+def part_lines(step, w, part_ms, burst, sustained):
+    """The per-call numbers of a timed region: pooled pairs/s and TFLOP/s, MaxSim fwd+bwd TFLOP/s, each as a
+    fraction of the burst bf16 peak (the calls run at full clock in a short timed region; the sustained
+    peak's fraction is given beside it)."""
+    p, m = step.p, step.m
+    pre = w.get("prefixes")
+    parts = {}
+    if p is not None:
+        pm = statistics.mean(part_ms["pooled"])
+        tf = pooled_flops(p, pre) / (pm * 1e-3) / 1e12
+        parts["pair_loss"] = {"ms": pm, "pairs_per_s": len(pre or [0]) * p.count * (p.count - 1) / (pm * 1e-3),
+                              "tflops": tf, "frac_of_peak": tf / burst, "frac_of_sustained_peak": tf / sustained,
+                              "N": p.count, "D": p.width}
+    if m is not None:
+        fm, bm = statistics.mean(part_ms["maxsim_fwd"]), statistics.mean(part_ms["maxsim_bwd"])
+        fwd, bwd = maxsim_fwd_flops(m, w.get("named")), maxsim_bwd_flops(m, w.get("named"))
+        tf = (fwd + bwd) / ((fm + bm) * 1e-3) / 1e12
+        active = step.active_pairs()
+        parts["maxsim"] = {"fwd_ms": fm, "bwd_ms": bm, "tflops_fwd_bwd": tf, "frac_of_peak": tf / burst,
+                           "frac_of_sustained_peak": tf / sustained, "fwd_tflops": fwd / (fm * 1e-3) / 1e12,
+                           "bwd_active_pairs": active,
+                           # one bf16 row gathered per active (query row, document) pair for each of dQ and dD
+                           "bwd_gathered_bytes": active * 4.0 * m.width,
+                           "bwd_gathered_gb_per_s": active * 4.0 * m.width / (bm * 1e-3) / 1e9}
+        if "score_loss" in part_ms:
+            parts["score_loss"] = {"ms": statistics.mean(part_ms["score_loss"])}
+    return parts
+
+
+def extra_part(name, seed, device, stream, flush, args, burst, sustained):
+    """A separately timed workload of the default run (the largest pooled config, the config-3 MaxSim), under
+    the same timing rules as the main line; returns its per-call numbers and its clocks."""
+    import torch
+    w = make_workload(name, seed)
+    step = Step(w, device, stream)
+    warm(step, stream, args.warmup)
+    step_ms, part_ms, clk, _ = timed_region(step, stream, flush, args.steps, device.index or 0)
+    out = part_lines(step, w, part_ms, burst, sustained)
+    out = out.get("pair_loss") or out.get("maxsim")
+    out.update({"workload": describe(name, w)["workload"], "ms_per_step": statistics.mean(step_ms), "clocks": clk,
+                "traffic": committed_traffic(name, "pooled" if w["pooled"] is not None else "maxsim")})
+    del step
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -632,70 +751,28 @@ def main():
     w = make_workload(args.workload, rank)   # weak scaling: every rank its own batch
     step = Step(w, device, stream)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    names = [n for n in ("pooled", "maxsim_fwd", "score_loss", "maxsim_bwd")
-             if (n == "pooled" and step.p is not None) or (n != "pooled" and step.m is not None and
-                                                          (n != "score_loss" or step.j is not None or
-                                                           step.named is not None))]
-
-    for _ in range(max(3, args.warmup)):
-        step.run()
-    stream.synchronize()
-    bad = [s for s in step.statuses() if s != 0]
-    if bad:
-        raise SystemExit(f"device status {bad} after warm-up")
+    warm(step, stream, args.warmup)
 
     # --- timed region: K steps, L2 flushed between steps (outside the per-step events) ---
-    ev = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for n in names}
-          for _ in range(args.steps)]
-    st_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    if pg is not None:
-        pg.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        clocks.mark(True)
-        wall0 = time.perf_counter()
-        for k in range(args.steps):
-            with torch.cuda.stream(stream):
-                flush.fill_(k & 0xFF)
-                st_ev[k][0].record(stream)
-                step.run(ev[k])
-                st_ev[k][1].record(stream)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - wall0
-        clocks.mark(False)
-    if pg is not None:
-        pg.barrier()
-    step_ms = [s.elapsed_time(e) for s, e in st_ev]
-    part_ms = {n: [ev[k][n][0].elapsed_time(ev[k][n][1]) for k in range(args.steps)] for n in names}
+    step_ms, part_ms, clocks, wall = timed_region(step, stream, flush, args.steps, local, pg)
     p, m = step.p, step.m
     pre = w.get("prefixes")
     flops = (pooled_flops(p, pre) if p is not None else 0.0) + \
             ((maxsim_fwd_flops(m, w.get("named")) + maxsim_bwd_flops(m, w.get("named"))) if m is not None else 0.0)
     ms, value = aggregate(pg, world, flops, statistics.mean(step_ms), device)
     burst, sustained, hbm, peak_src = peaks()
-    parts = {}
-    if p is not None:
-        pm = statistics.mean(part_ms["pooled"])
-        parts["pair_loss"] = {"ms": pm, "pairs_per_s": len(pre or [0]) * p.count * (p.count - 1) / (pm * 1e-3),
-                              "tflops": pooled_flops(p, pre) / (pm * 1e-3) / 1e12,
-                              "frac_of_peak": pooled_flops(p, pre) / (pm * 1e-3) / 1e12 / sustained}
-    if m is not None:
-        fm, bm = statistics.mean(part_ms["maxsim_fwd"]), statistics.mean(part_ms["maxsim_bwd"])
-        tf = (maxsim_fwd_flops(m, w.get("named")) + maxsim_bwd_flops(m, w.get("named"))) / ((fm + bm) * 1e-3) / 1e12
-        parts["maxsim"] = {"fwd_ms": fm, "bwd_ms": bm, "tflops_fwd_bwd": tf, "frac_of_peak": tf / sustained,
-                           "fwd_tflops": maxsim_fwd_flops(m, w.get("named")) / (fm * 1e-3) / 1e12,
-                           "bwd_gathered_gb_per_s": maxsim_bwd_flops(m, w.get("named")) / (bm * 1e-3) / 1e9}
-        if step.j is not None or step.named is not None:
-            parts["score_loss"] = {"ms": statistics.mean(part_ms["score_loss"])}
+    parts = part_lines(step, w, part_ms, burst, sustained)
 
-    # roofline: the dominant kernel (by time) of the step
+    # roofline: the dominant kernel (by time) of the step, against the burst peak (a short timed region at
+    # full clock); the sustained peak's fraction beside it
     if m is not None:
         fm = statistics.mean(part_ms["maxsim_fwd"])
         achieved = maxsim_fwd_flops(m, w.get("named")) / (fm * 1e-3) / 1e12
         roofline = {"kernel": "maxsim forward (maxsim_scores call: forward tile kernel + its schedule, tape "
                               "checks and query sums)",
-                    "bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
-                    "frac": achieved / sustained, "peak_source": f"{peak_src} bf16 sustained",
+                    "bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
+                    "frac": achieved / burst, "peak_source": f"{peak_src} bf16 burst",
+                    "frac_of_sustained_peak": achieved / sustained,
                     "traffic": committed_traffic(args.workload),
                     "algorithmic_per_launch": maxsim_fwd_flops(m, w.get("named"))}
     else:
@@ -704,11 +781,13 @@ def main():
         call = ("pair_loss_sigmoid_groups_fwd_bwd" if w.get("groups") else
                 "pair_loss_sigmoid_matryoshka_fwd_bwd" if pre else "pair_loss_sigmoid_fwd_bwd")
         roofline = {"kernel": f"pooled fused block kernel ({call} call)", "bound": "tensor",
-                    "achieved": achieved, "peak": sustained, "unit": "TFLOP/s", "frac": achieved / sustained,
-                    "peak_source": f"{peak_src} bf16 sustained", "traffic": committed_traffic(args.workload, "pooled"),
+                    "achieved": achieved, "peak": burst, "unit": "TFLOP/s", "frac": achieved / burst,
+                    "peak_source": f"{peak_src} bf16 burst", "frac_of_sustained_peak": achieved / sustained,
+                    "traffic": committed_traffic(args.workload, "pooled"),
                     "algorithmic_per_launch": pooled_flops(p, pre)}
 
-    # end to end through the C ABI with host buffers: inputs copied in, losses read back, every step
+    # end to end through the C ABI with host buffers: every input copied in from pinned host memory and every
+    # result (losses, dE, scores, dQ, dD) copied back, each step
     e2e = None
     if not args.no_e2e:
         h2d = 0
@@ -736,10 +815,19 @@ def main():
         e2e_ms = max_over_ranks(pg, e2e_ms, device)
         e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        del outs_host
 
     bad = [s for s in step.statuses() if s != 0]
     if bad:
         raise SystemExit(f"device status {bad}")
+    launches = step.launches_per_step() * args.steps
+
+    # the largest pooled config and the config-3 MaxSim, timed on their own (rank 0, single GPU)
+    if args.workload == "joint" and not args.no_extra_parts and world == 1:
+        del step
+        torch.cuda.empty_cache()
+        parts["pooled_config4"] = extra_part("pooled4", rank, device, stream, flush, args, burst, sustained)
+        parts["maxsim_config3"] = extra_part("maxsim3", rank, device, stream, flush, args, burst, sustained)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -754,9 +842,8 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg, "parts": parts,
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": step.launches_per_step() * args.steps,
-                "clocks": clocks.summary(), "wall_s_timed": wall}
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "clocks": clocks, "wall_s_timed": wall}
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
