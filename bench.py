@@ -255,8 +255,9 @@ class Step:
         """Kernels of this library one step launches (mirrors the launch code of csrc/)."""
         n = 0
         if self.p is not None:
-            n += 1 + (1 if self.ign is not None else 0)   # edge validation, one per edge set given
-            n += 1 + 3 + 1 + 1 + 1 + 1 + 1                # in-degree, 3 scans, fill, sort, count, scan, emit
+            sets = 1 + (1 if self.ign is not None else 0)
+            n += sets                                     # edge validation, one per edge set given
+            n += 1 + sets + 1 + 1 + 1                     # in-degree, a scan per set, fill, sort, merge
             if self.groups:
                 n += 1 + 3                                # group validation, fused block kernel, final reduction
             elif self.prefixes:                           # per prefix: normalise, fused, 2 reductions, gradient

@@ -34,7 +34,6 @@ struct PooledWorkspace {
     uint32_t *tin_off;     // [3][n+1] transposed offsets
     uint32_t *tin_ids;     // [E_total]  (set s at tin_base[s])
     float *tin_w;          // [E_total]
-    uint32_t *rel_cnt;     // [n]
     uint32_t *rel_off;     // [n+1]
     RelEntry *rel;         // [2 E_total + n]
     float *partials;       // [pooled_partial_slots(n)][4]

@@ -84,42 +84,47 @@ __global__ void count_indegree_kernel(EdgeSet a, EdgeSet r, EdgeSet g, int n, ui
 }
 
 // Exclusive scan of `count` values into out[0..count], starting at `base`;
-// one block of 1024 threads.
-__global__ void scan_kernel(const uint32_t *in, uint32_t *out, int count, uint32_t base, const int32_t *status) {
+// one block of 1024 threads.  Each warp scans a contiguous range in coalesced
+// 32-value steps (shuffles and a running carry, no block barrier), the warp
+// totals are scanned once, and a second coalesced pass adds each warp's offset.
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(const uint32_t *in, uint32_t *out, int count,
+                                                            uint32_t base, const int32_t *status) {
     if (read_status(status) != 0) return;
-    __shared__ uint32_t warp_sums[32];
-    __shared__ uint32_t carry_s;
-    uint32_t carry = base;
+    constexpr int kWarps = kScanThreads / 32;
+    __shared__ uint32_t warp_off[kWarps];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    for (int base = 0; base < count; base += blockDim.x) {
-        const int i = base + threadIdx.x;
-        const uint32_t v = i < count ? in[i] : 0u;
+    const int per = ((count + kWarps - 1) / kWarps + 31) & ~31;
+    const int lo = min(count, w * per), hi = min(count, lo + per);
+    uint32_t carry = 0;
+    for (int b = lo; b < hi; b += 32) {
+        const int i = b + lane;
+        const uint32_t v = i < hi ? in[i] : 0u;
         uint32_t x = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
             if (lane >= o) x += y;
         }
-        if (lane == 31) warp_sums[w] = x;
-        __syncthreads();
-        if (w == 0) {
-            uint32_t s = lane < (blockDim.x >> 5) ? warp_sums[lane] : 0u;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
-                if (lane >= o) s += y;
-            }
-            warp_sums[lane] = s;  // inclusive prefix of warp totals
-        }
-        __syncthreads();
-        const uint32_t before = (w > 0 ? warp_sums[w - 1] : 0u) + x - v;
-        if (i < count) out[i] = carry + before;
-        if (threadIdx.x == blockDim.x - 1) carry_s = carry + before + v;
-        __syncthreads();
-        carry = carry_s;
-        __syncthreads();
+        if (i < hi) out[i] = carry + x - v;
+        carry += __shfl_sync(0xffffffffu, x, 31);
     }
-    if (threadIdx.x == 0) out[count] = carry;
+    if (lane == 0) warp_off[w] = carry;
+    __syncthreads();
+    if (w == 0) {
+        const uint32_t t = warp_off[lane];
+        uint32_t x = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        warp_off[lane] = x - t;   // exclusive
+        if (lane == 31) out[count] = base + x;
+    }
+    __syncthreads();
+    const uint32_t add = base + warp_off[w];
+    for (int i = lo + lane; i < hi; i += 32) out[i] += add;
 }
 
 __global__ void fill_transpose_kernel(EdgeSet a, EdgeSet r, EdgeSet g, int n, const uint32_t *tin_off,
@@ -142,12 +147,14 @@ __global__ void fill_transpose_kernel(EdgeSet a, EdgeSet r, EdgeSet g, int n, co
 }
 
 // Sorts every transposed row by source id (rows are short: insertion sort).
-__global__ void sort_rows_kernel(const uint32_t *tin_off, uint32_t *tin_ids, float *tin_w, int n,
+// `present`: bit s set when edge set s was given (the others have no rows).
+__global__ void sort_rows_kernel(const uint32_t *tin_off, uint32_t *tin_ids, float *tin_w, int n, int present,
                                  const int32_t *status) {
     if (read_status(status) != 0) return;
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= 3 * n) return;
     const int s = idx / n, j = idx % n;
+    if (!((present >> s) & 1)) return;
     const uint32_t a = tin_off[static_cast<size_t>(s) * (n + 1) + j];
     const uint32_t b = tin_off[static_cast<size_t>(s) * (n + 1) + j + 1];
     for (uint32_t k = a + 1; k < b; ++k) {
@@ -238,22 +245,46 @@ __device__ uint32_t merge_row(int i, EdgeSet a, EdgeSet r, EdgeSet g, int n, con
     return count;
 }
 
-__global__ void merge_count_kernel(EdgeSet a, EdgeSet r, EdgeSet g, int n, const uint32_t *tin_off,
-                                   const uint32_t *tin_ids, const float *tin_w, uint32_t *rel_cnt,
-                                   const int32_t *status) {
-    if (read_status(status) != 0) return;
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    rel_cnt[i] = merge_row<false>(i, a, r, g, n, tin_off, tin_ids, tin_w, 0, 0.f, nullptr);
+// Row i's merged list is written at rel_off[i] = the number of list slots of
+// the rows before it, where row i has one slot per edge it is the source or the
+// target of (in any set) plus one for the diagonal: an upper bound on its
+// distinct columns, so no counting pass is needed.  Slots past the row's
+// distinct columns hold sentinel entries (column 0xFFFFFFFF, past every real
+// column), which the tile kernel never reaches.  rel_off[i] follows from the
+// edge sets' offsets and the transposed offsets, both prefix sums already.
+__device__ __forceinline__ uint32_t rel_slots_before(EdgeSet a, EdgeSet r, EdgeSet g, int n, const uint32_t *tin_off,
+                                                     const uint32_t *tin_base, int i) {
+    const EdgeSet sets[3] = {a, r, g};
+    uint32_t before = static_cast<uint32_t>(i);
+#pragma unroll
+    for (int s = 0; s < 3; ++s)
+        if (sets[s].offsets)
+            before += static_cast<uint32_t>(sets[s].offsets[i]) +
+                      (tin_off[static_cast<size_t>(s) * (n + 1) + i] - tin_base[s]);
+    return before;
 }
 
+struct TinBase {
+    uint32_t v[3];   // where each set's transposed ids start in the shared id array
+};
+
 __global__ void merge_emit_kernel(EdgeSet a, EdgeSet r, EdgeSet g, int n, const uint32_t *tin_off,
-                                  const uint32_t *tin_ids, const float *tin_w, const uint32_t *rel_off, RelEntry *rel,
-                                  int named, float ambient, const int32_t *status) {
+                                  const uint32_t *tin_ids, const float *tin_w, TinBase tb, uint32_t *rel_off,
+                                  RelEntry *rel, int named, float ambient, const int32_t *status) {
     if (read_status(status) != 0) return;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
-    merge_row<true>(i, a, r, g, n, tin_off, tin_ids, tin_w, named, ambient, rel + rel_off[i]);
+    const uint32_t o0 = rel_slots_before(a, r, g, n, tin_off, tb.v, i);
+    const uint32_t o1 = rel_slots_before(a, r, g, n, tin_off, tb.v, i + 1);
+    rel_off[i] = o0;
+    if (i == n - 1) rel_off[n] = o1;
+    const uint32_t used = merge_row<true>(i, a, r, g, n, tin_off, tin_ids, tin_w, named, ambient, rel + o0);
+    RelEntry sentinel;
+    sentinel.col = kNone;
+    sentinel.flags = 0;
+    sentinel.w_out = 0.f;
+    sentinel.w_in = 0.f;
+    for (uint32_t k = o0 + used; k < o1; ++k) rel[k] = sentinel;
 }
 
 inline unsigned blocks_for(long long n, int threads) { return static_cast<unsigned>((n + threads - 1) / threads); }
@@ -276,7 +307,6 @@ PooledWorkspace carve_pooled_workspace(void *base, size_t n, size_t width, size_
     w.tin_off = reinterpret_cast<uint32_t *>(take(3 * (n + 1) * sizeof(uint32_t)));
     w.tin_ids = reinterpret_cast<uint32_t *>(take((edges_total + 1) * sizeof(uint32_t)));
     w.tin_w = reinterpret_cast<float *>(take((edges_total + 1) * sizeof(float)));
-    w.rel_cnt = reinterpret_cast<uint32_t *>(take(n * sizeof(uint32_t)));
     w.rel_off = reinterpret_cast<uint32_t *>(take((n + 1) * sizeof(uint32_t)));
     w.rel = reinterpret_cast<RelEntry *>(take((2 * edges_total + n) * sizeof(RelEntry)));
     w.partials = reinterpret_cast<float *>(
@@ -312,25 +342,29 @@ cudaError_t launch_relation_prep(const EdgeSet sets[3], int n, int named, float 
         return err;
     count_indegree_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(sets[0], sets[1], sets[2], n, ws.indeg, status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    // Transposed offsets of set s index one shared id array, after the sets before it.
+    // Transposed offsets of set s index one shared id array, after the sets before it (absent sets have
+    // no transposed rows and are never read).
     uint64_t base = 0;
+    TinBase tb;
     for (int s = 0; s < 3; ++s) {
-        scan_kernel<<<1, 1024, 0, stream>>>(ws.indeg + static_cast<size_t>(s) * n,
-                                            ws.tin_off + static_cast<size_t>(s) * (n + 1), n,
-                                            static_cast<uint32_t>(base), status);
+        tb.v[s] = static_cast<uint32_t>(base);
+        if (!sets[s].offsets) continue;
+        scan_kernel<<<1, kScanThreads, 0, stream>>>(ws.indeg + static_cast<size_t>(s) * n,
+                                                    ws.tin_off + static_cast<size_t>(s) * (n + 1), n,
+                                                    static_cast<uint32_t>(base), status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
-        base += sets[s].offsets ? sets[s].edges : 0;
+        base += sets[s].edges;
     }
     if ((err = cudaMemsetAsync(ws.indeg, 0, 3 * static_cast<size_t>(n) * sizeof(uint32_t), stream)) != cudaSuccess)
         return err;
     fill_transpose_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(sets[0], sets[1], sets[2], n, ws.tin_off, ws.indeg,
                                                                    ws.tin_ids, ws.tin_w, status);
-    sort_rows_kernel<<<blocks_for(3LL * n, 256), 256, 0, stream>>>(ws.tin_off, ws.tin_ids, ws.tin_w, n, status);
-    merge_count_kernel<<<blocks_for(n, 128), 128, 0, stream>>>(sets[0], sets[1], sets[2], n, ws.tin_off, ws.tin_ids,
-                                                                ws.tin_w, ws.rel_cnt, status);
-    scan_kernel<<<1, 1024, 0, stream>>>(ws.rel_cnt, ws.rel_off, n, 0u, status);
+    const int present = (sets[0].offsets ? 1 : 0) | (sets[1].offsets ? 2 : 0) | (sets[2].offsets ? 4 : 0);
+    sort_rows_kernel<<<blocks_for(3LL * n, 256), 256, 0, stream>>>(ws.tin_off, ws.tin_ids, ws.tin_w, n, present,
+                                                                    status);
     merge_emit_kernel<<<blocks_for(n, 128), 128, 0, stream>>>(sets[0], sets[1], sets[2], n, ws.tin_off, ws.tin_ids,
-                                                               ws.tin_w, ws.rel_off, ws.rel, named, ambient, status);
+                                                               ws.tin_w, tb, ws.rel_off, ws.rel, named, ambient,
+                                                               status);
     return cudaGetLastError();
 }
 
