@@ -479,7 +479,7 @@ def peaks():
 
 # Committed DRAM-traffic records: file under profiles/ -> the kernel sources its counters were taken on.
 TRAFFIC_RECORDS = {
-    "maxsim": ("maxsim_forward_traffic.json", ("maxsim.cu", "cli_device.cuh")),
+    "maxsim": ("maxsim_forward_traffic.json", ("maxsim.cu", "cli_device.cuh", "compact.cuh")),
     "pooled": ("pooled_fused_traffic.json", ("pair_loss.cu", "cli_device.cuh")),
 }
 
