@@ -229,9 +229,14 @@ __global__ void __launch_bounds__(256, NBLK <= 2 ? 4 : 2) dq_kernel(MaxSimBwdLau
 // a bucket because each bucket is summed by one group in list order, and the
 // list order is the scatter order (atomic slot claims), which may vary between
 // runs: dD is reproducible to rounding, not bit for bit.
-constexpr int kDsThreads = 512;
-constexpr int kDsMaxRows = 4096;
-constexpr int kDsChunk = 16384;
+// One CTA of 1024 threads per SM, so the list holds 32800 query rows (160 KB of
+// shared memory in all): two chunks cover 65600 query rows, and every chunk past
+// the first pays its sort passes again and a read-modify-write of the rows (with
+// two CTAs of 512 threads and 16384-row chunks the config-5 backward took 3.28
+// ms, with this 2.91 ms).
+constexpr int kDsThreads = 1024;
+constexpr int kDsMaxRows = 2048;
+constexpr int kDsChunk = 32800;
 constexpr int kDsMaxTable = 4096;
 constexpr int kDsBatch = 8;   // argmax entries per thread in flight in the histogram and scatter passes
 
@@ -290,7 +295,7 @@ __device__ __forceinline__ void dd_row_sum(const MaxSimBwdLaunch &L, const uint3
 // NB: 128-feature blocks of the width (ceil(width / 128)); kDsUnroll: bucket
 // entries in flight per 8-lane group.
 template <int NB, int kDsUnroll>
-__global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch L) {
+__global__ void __launch_bounds__(kDsThreads, 1) dd_sort_kernel(MaxSimBwdLaunch L) {
     extern __shared__ uint8_t ds_raw[];
     uint32_t *cnt = reinterpret_cast<uint32_t *>(ds_raw);            // [kDsMaxRows] counts, then cursors
     uint32_t *off = cnt + kDsMaxRows;                                  // [kDsMaxRows + 1] bucket starts
@@ -348,7 +353,7 @@ __global__ void __launch_bounds__(kDsThreads, 2) dd_sort_kernel(MaxSimBwdLaunch 
             __syncthreads();
             // exclusive scan of cnt[0..wrows) into off[], then cnt[] becomes the cursor
             {
-                constexpr int kPer = kDsMaxRows / kDsThreads;   // 8 entries per thread
+                constexpr int kPer = kDsMaxRows / kDsThreads;   // entries per thread
                 uint32_t v[kPer], sum = 0;
 #pragma unroll
                 for (int i = 0; i < kPer; ++i) {
