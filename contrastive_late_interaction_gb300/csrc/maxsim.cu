@@ -509,7 +509,16 @@ __global__ void query_sum_kernel(const float *mval, const uint64_t *q_off, int n
         const uint64_t a = q_off[q], b = q_off[q + 1];
         const float *m = mval + static_cast<long long>(d) * rows_q;
         float s = 0.f, lowest = INFINITY;
-        for (uint64_t t = a; t < b; ++t) {
+        uint64_t t = a;
+        for (; t + 4 <= b; t += 4) {   // four loads in flight, the sum still in row order
+            const float v0 = m[t], v1 = m[t + 1], v2 = m[t + 2], v3 = m[t + 3];
+            s += v0;
+            s += v1;
+            s += v2;
+            s += v3;
+            lowest = fminf(fminf(lowest, fminf(v0, v1)), fminf(v2, v3));
+        }
+        for (; t < b; ++t) {
             const float v = m[t];
             s += v;
             lowest = fminf(lowest, v);
