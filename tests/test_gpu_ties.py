@@ -47,3 +47,18 @@ def test_maxsim_exact_ties_take_the_lowest_row(regime, d_len, mean):
     dq, dd = oracle.maxsim_backward(m.q_offsets, m.q, m.d_offsets, m.d, arg, m.d_scores, mean)
     assert rel_l2(g["dq"], dq) <= GRAD_RL2
     assert rel_l2(g["dd"], dd) <= GRAD_RL2
+
+
+def test_maxsim_fixup_list_overflow_scans_every_maximum():
+    """More rows with a non-positive maximum than the fix-up list holds (2^18 entries): the fix-up scans
+    every maximum instead, and every argmax is still the oracle's (the lowest row)."""
+    m = synth.maxsim_ties(12, "negative", nq=160, nd=60, q_len=(20, 50), d_len=(1, 40))
+    entries = int(m.q_offsets[-1]) * m.nd
+    assert entries > (1 << 18)
+    g = run_maxsim(m)
+    assert g["status_f"] == 0 and g["status_b"] == 0
+    s, arg, gap = oracle.maxsim_forward(m.q_offsets, m.q, m.d_offsets, m.d)
+    check_scores(g["scores"], s)
+    assert np.all(s < 0)
+    wrong = np.count_nonzero(g["argmax"] != arg)
+    assert wrong == 0, f"{wrong} of {arg.size} argmax entries differ"
