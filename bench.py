@@ -333,9 +333,9 @@ class Step:
                                         workspace=self.b_ws, device_status=self.b_st, stream=self.stream)
                 rec("maxsim_bwd", 1)
 
-    def upload(self):
-        """Host -> device copies of every input of a step (pinned memory, the step's stream)."""
-        with self.torch.cuda.stream(self.stream):
+    def upload(self, stream=None):
+        """Host -> device copies of every input of a step (pinned memory; the step's stream, or `stream`)."""
+        with self.torch.cuda.stream(stream if stream is not None else self.stream):
             for k, h in self.host.items():
                 self.dev_in[k].copy_(h, non_blocking=True)
         return sum(h.numel() * h.element_size() for h in self.host.values())
@@ -737,6 +737,88 @@ def extra_part(name, seed, device, stream, flush, args, burst, sustained):
     return out
 
 
+def e2e_serial(step, stream, steps, pg, device):
+    """Per step on one stream: the inputs in, the step, the results out.  Returns (ms per step, bytes in,
+    bytes out)."""
+    import torch
+    outs_host = [torch.empty(d.shape, dtype=d.dtype).pin_memory() for d in step.results()]
+    for _ in range(2):
+        step.upload()
+        step.run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg is not None:
+        pg.barrier()
+    h2d = d2h = 0
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            h2d = step.upload()
+            step.run()
+            for h, d in zip(outs_host, step.results()):
+                h.copy_(d, non_blocking=True)
+            d2h = sum(h.numel() * h.element_size() for h in outs_host)
+        e1.record(stream)
+    stream.synchronize()
+    ms = max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3) / steps
+    return max_over_ranks(pg, ms, device), h2d, d2h
+
+
+def e2e_pipelined(steps2, stream, steps, pg, device):
+    """Steps alternate between two device buffer sets: step k's inputs go in on one copy stream once step
+    k - 2 (the last user of its set) has finished, the step runs on `stream` once they are in and step
+    k - 2's results are out, and its results come back on a second copy stream, so the copies of one step
+    overlap the compute of the next.  Every step still copies all of its inputs in and all of its results
+    out inside the timed region.  Returns (ms per step, bytes in, bytes out)."""
+    import torch
+    h2d_s, d2h_s = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    outs_host = [[torch.empty(d.shape, dtype=d.dtype).pin_memory() for d in st.results()] for st in steps2]
+    ev = lambda: torch.cuda.Event()
+    copied_in = [ev(), ev()]
+    computed = [ev(), ev()]
+    copied_out = [ev(), ev()]
+    sizes = {}
+
+    def one(k):
+        i = k % 2
+        st = steps2[i]
+        if k >= 2:
+            h2d_s.wait_event(computed[i])
+        sizes["in"] = st.upload(h2d_s)
+        copied_in[i].record(h2d_s)
+        stream.wait_event(copied_in[i])
+        if k >= 2:
+            stream.wait_event(copied_out[i])
+        st.run()
+        computed[i].record(stream)
+        d2h_s.wait_event(computed[i])
+        with torch.cuda.stream(d2h_s):
+            for h, d in zip(outs_host[i], st.results()):
+                h.copy_(d, non_blocking=True)
+        copied_out[i].record(d2h_s)
+        sizes["out"] = sum(h.numel() * h.element_size() for h in outs_host[i])
+
+    for k in range(4):
+        one(k)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg is not None:
+        pg.barrier()
+    t0 = time.perf_counter()
+    e0.record(h2d_s)
+    stream.wait_event(e0)
+    d2h_s.wait_event(e0)
+    for k in range(steps):
+        one(k + 4)
+    stream.wait_event(copied_out[(steps + 3) % 2])
+    stream.wait_event(copied_out[(steps + 2) % 2])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3) / steps
+    return max_over_ranks(pg, ms, device), sizes["in"], sizes["out"]
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -791,32 +873,20 @@ def main():
     # result (losses, dE, scores, dQ, dD) copied back, each step
     e2e = None
     if not args.no_e2e:
-        h2d = 0
-        d2h = 0
-        outs_host = [torch.empty(d.shape, dtype=d.dtype).pin_memory() for d in step.results()]
-        for _ in range(2):
-            step.upload()
-            step.run()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if pg is not None:
-            pg.barrier()
-        t0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(args.steps):
-                h2d = step.upload()
-                step.run()
-                for h, d in zip(outs_host, step.results()):
-                    h.copy_(d, non_blocking=True)
-                d2h = sum(h.numel() * h.element_size() for h in outs_host)
-            e1.record(stream)
-        stream.synchronize()
-        e2e_ms = max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3) / args.steps
-        e2e_ms = max_over_ranks(pg, e2e_ms, device)
+        serial_ms, _, _ = e2e_serial(step, stream, args.steps, pg, device)
+        step2 = Step(w, device, stream)   # the second device buffer set of the pipelined copies
+        e2e_ms, h2d, d2h = e2e_pipelined((step, step2), stream, args.steps, pg, device)
+        bad2 = [s for s in step2.statuses() if s != 0]
+        if bad2:
+            raise SystemExit(f"device status {bad2}")
+        del step2
+        torch.cuda.empty_cache()
         e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-        del outs_host
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "copies": "step k+1's inputs copied in and step k's results copied out on two copy streams while "
+                         "step k+1 computes (two device buffer sets)",
+               "serial_ms_per_step": serial_ms,
+               "serial_value": world * flops / (serial_ms * 1e-3) / 1e12}
 
     bad = [s for s in step.statuses() if s != 0]
     if bad:
