@@ -108,12 +108,15 @@ __global__ void __launch_bounds__(256, NBLK <= 2 ? 4 : 2) dq_kernel(MaxSimBwdLau
     // c = 0 for every query), else all of them in order (no list indirection in the loads).
     const int n_docs = L.d_list ? static_cast<int>(*L.d_count) : L.nd;
     const bool use_list = n_docs < L.nd;
-    // The loads that resolve the i-th document (its id, argmax entry and c) ...
+    // The i-th document's id: from the list (a load, issued a step before the id is used, so that the
+    // loads it addresses never wait on it) or i itself.
+    auto id_at = [&](int i) { return use_list && i < n_docs ? static_cast<int>(__ldg(L.d_list + i)) : i; };
+    // The loads that resolve the i-th document (its argmax entry and c, given its id) ...
     int a_n = 0, d_n = 0;
     float c_n = 0.f;
-    auto fetch = [&](int i) {
+    auto fetch = [&](int i, int id) {
         if (i < n_docs) {
-            d_n = use_list ? static_cast<int>(__ldg(L.d_list + i)) : i;
+            d_n = id;
             a_n = __ldg(amcol + static_cast<long long>(d_n) * L.ld_argmax);
             c_n = __ldg(dsrow + d_n);
         }
@@ -194,12 +197,15 @@ __global__ void __launch_bounds__(256, NBLK <= 2 ? 4 : 2) dq_kernel(MaxSimBwdLau
     };
     unsigned long long src;
     float c;
-    fetch(sub);
+    fetch(sub, id_at(sub));
     finish(sub, src, c);
+    int id_next = id_at(kDqUnroll + sub);
     for (int d0 = 0; d0 < (warp_idle ? 0 : n_docs); d0 += kDqUnroll) {
-        fetch(d0 + kDqUnroll + sub);   // the next step's resolution, in flight during this step
+        const int id_after = id_at(d0 + 2 * kDqUnroll + sub);   // the id two steps on, in flight meanwhile
+        fetch(d0 + kDqUnroll + sub, id_next);   // the next step's resolution, in flight during this step
         step(src, c);
         finish(d0 + kDqUnroll + sub, src, c);
+        id_next = id_after;
     }
     if (!row_ok) return;
     float *dst = L.dq + static_cast<long long>(t) * L.width;
