@@ -509,20 +509,25 @@ __global__ void query_sum_kernel(const float *mval, const uint64_t *q_off, int n
         const uint64_t a = q_off[q], b = q_off[q + 1];
         const float *m = mval + static_cast<long long>(d) * rows_q;
         float s = 0.f, lowest = INFINITY;
-        uint64_t t = a;
-        for (; t + 4 <= b; t += 4) {   // four loads in flight, the sum still in row order
-            const float v0 = m[t], v1 = m[t + 1], v2 = m[t + 2], v3 = m[t + 3];
-            s += v0;
-            s += v1;
-            s += v2;
-            s += v3;
-            lowest = fminf(fminf(lowest, fminf(v0, v1)), fminf(v2, v3));
-        }
-        for (; t < b; ++t) {
-            const float v = m[t];
+        auto add = [&](float v) {
             s += v;
             lowest = fminf(lowest, v);
+        };
+        // In row order: single maxima up to a 16-byte boundary of the workspace, then 16-byte loads (two
+        // in flight), then the rest.
+        uint64_t t = a;
+        const uint64_t at = static_cast<uint64_t>(d) * static_cast<uint64_t>(rows_q);   // m[t] is mval[at + t]
+        for (; t < b && ((at + t) & 3u) != 0; ++t) add(m[t]);
+        for (; t + 8 <= b; t += 8) {
+            const float4 u = *reinterpret_cast<const float4 *>(m + t), w = *reinterpret_cast<const float4 *>(m + t + 4);
+            add(u.x); add(u.y); add(u.z); add(u.w);
+            add(w.x); add(w.y); add(w.z); add(w.w);
         }
+        for (; t + 4 <= b; t += 4) {
+            const float4 u = *reinterpret_cast<const float4 *>(m + t);
+            add(u.x); add(u.y); add(u.z); add(u.w);
+        }
+        for (; t < b; ++t) add(m[t]);
         if (!(lowest >= 1.17549435e-38f)) {   // rare: some row's scores all <= 0 over the document, or subnormal
             for (uint64_t t = a; t < b; ++t) {
                 if (m[t] >= 1.17549435e-38f) continue;
