@@ -88,6 +88,8 @@ template <int NBLK>   // 64-feature blocks of the width (1..4)
 // Up to width 128, at most 64 registers, so four blocks (32 warps) share an SM: the gathers are
 // latency-bound.
 __global__ void __launch_bounds__(256, NBLK <= 2 ? 4 : 2) dq_kernel(MaxSimBwdLaunch L) {
+    // dD (launched next) reads nothing dQ writes: let its CTAs start on the SMs this grid's last CTAs leave.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (read_status(L.status) != 0) return;
     const int t = blockIdx.x * kDqRows + (threadIdx.x >> 3);
     const int sub = threadIdx.x & 7;
@@ -491,6 +493,27 @@ __global__ void __launch_bounds__(256) named_backward_kernel(MaxSimBwdLaunch L, 
 
 }  // namespace ms
 
+// dD as a programmatic dependent of the dQ grid launched just before it on the
+// same stream: its CTAs may start once every dQ CTA has started (dQ signals at
+// its start), filling the SMs that dQ's last wave leaves idle.  dD reads only
+// what the kernels before dQ wrote (they completed before dQ began), never
+// dQ's output, so it needs no wait on the dQ grid; the stream's later work
+// still waits for both.
+template <typename K>
+cudaError_t launch_after_dq(K kernel, const MaxSimBwdLaunch &L, size_t smem, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(L.nd));
+    cfg.blockDim = dim3(ms::kDsThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, L);
+}
+
 cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream) {
     using namespace ms;
     cudaError_t err;
@@ -521,13 +544,14 @@ cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream
         if ((err = cudaFuncSetAttribute(dd_sort_kernel<1, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(ds_smem))) != cudaSuccess)
             return err;
-        dd_sort_kernel<1, 4><<<L.nd, kDsThreads, ds_smem, stream>>>(L);
+        err = launch_after_dq(dd_sort_kernel<1, 4>, L, ds_smem, stream);
     } else {
         if ((err = cudaFuncSetAttribute(dd_sort_kernel<2, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(ds_smem))) != cudaSuccess)
             return err;
-        dd_sort_kernel<2, 1><<<L.nd, kDsThreads, ds_smem, stream>>>(L);
+        err = launch_after_dq(dd_sort_kernel<2, 1>, L, ds_smem, stream);
     }
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
