@@ -267,7 +267,8 @@ class Step:
         if self.m is not None:
             n += 2 + 1 + 1 + 1 + 1                        # 2 tape validations, schedule, forward, query sums, fix-up
             if not self.named:
-                n += 2 + 1 + 1 + 1                        # 2 tape validations, row->query map, dQ, dD
+                n += 2 + 1 + 1 + 1 + 1                    # 2 tape validations, activity flags and row->query map,
+                                                          # active-document list, dQ, dD
             if self.named:
                 n += 2 + 1 + 1                            # 2 tape validations, pair validation, named backward
                 n += 1 + 1 + 1                            # pair validation, item marks, compaction

@@ -22,11 +22,12 @@ namespace ms {
 
 // q_active[q] = 1 when some c(q, d) is nonzero, d_active[d] = 1 when some
 // c(q, d) is (one block per query; both zeroed beforehand, every writer
-// writes 1).
-__global__ void active_kernel(const float *d_scores, long long ld_ds, int nd, uint8_t *q_active, uint8_t *d_active,
-                              const int32_t *status) {
+// writes 1); the block also maps its query's rows to the query.
+__global__ void active_kernel(const float *d_scores, long long ld_ds, int nd, const uint64_t *q_off, int32_t *qmap,
+                              uint8_t *q_active, uint8_t *d_active, const int32_t *status) {
     if (read_status(status) != 0) return;
     const int q = blockIdx.x;
+    for (uint64_t t = q_off[q] + threadIdx.x; t < q_off[q + 1]; t += blockDim.x) qmap[t] = q;
     const float *row = d_scores + static_cast<long long>(q) * ld_ds;
     int any = 0;
     for (int d = threadIdx.x; d < nd; d += blockDim.x)
@@ -35,19 +36,6 @@ __global__ void active_kernel(const float *d_scores, long long ld_ds, int nd, ui
             d_active[d] = 1;
         }
     if (__syncthreads_or(any) && threadIdx.x == 0) q_active[q] = 1;
-}
-
-// The dD rows of a document no query scores are zero (its argmax entries are
-// not read).
-__global__ void dd_zero_kernel(MaxSimBwdLaunch L) {
-    if (read_status(L.status) != 0) return;
-    const int d = blockIdx.x;
-    if (L.d_active[d]) return;
-    const uint64_t o0 = L.d_off[d];
-    const int dl = static_cast<int>(L.d_off[d + 1] - o0);
-    float4 *dst = reinterpret_cast<float4 *>(L.dd + static_cast<long long>(o0) * L.width);
-    const long long n4 = static_cast<long long>(dl) * L.width / 4;
-    for (long long i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 __global__ void qmap_kernel(const uint64_t *q_off, int nq, int32_t *qmap, const int32_t *status) {
@@ -313,7 +301,13 @@ __global__ void __launch_bounds__(kDsThreads, 1) dd_sort_kernel(MaxSimBwdLaunch 
     __shared__ uint32_t warp_sums[kDsThreads / 32];
     if (read_status(L.status) != 0) return;
     const int d = blockIdx.x;
-    if (L.d_active && !L.d_active[d]) return;   // dd_zero_kernel writes its rows
+    if (L.d_active && !L.d_active[d]) {   // no query scores it: its rows are zero (its argmax entries are not read)
+        const uint64_t z0 = L.d_off[d];
+        float4 *dst = reinterpret_cast<float4 *>(L.dd + static_cast<long long>(z0) * L.width);
+        const long long n4 = static_cast<long long>(L.d_off[d + 1] - z0) * L.width / 4;
+        for (long long i = threadIdx.x; i < n4; i += kDsThreads) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint64_t o0 = L.d_off[d];
     const int dl = static_cast<int>(L.d_off[d + 1] - o0);
@@ -517,18 +511,18 @@ cudaError_t launch_after_dq(K kernel, const MaxSimBwdLaunch &L, size_t smem, cud
 cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream) {
     using namespace ms;
     cudaError_t err;
-    qmap_kernel<<<(L.nq + 255) / 256, 256, 0, stream>>>(L.q_off, L.nq, L.qmap, L.status);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    if (L.q_active) {
+    if (L.q_active) {   // the activity flags (and the row -> query map), then the list of active documents
         if ((err = cudaMemsetAsync(L.q_active, 0, L.nq, stream)) != cudaSuccess ||
             (err = cudaMemsetAsync(L.d_active, 0, L.nd, stream)) != cudaSuccess)
             return err;
-        active_kernel<<<L.nq, 256, 0, stream>>>(L.d_scores, L.ld_ds, L.nd, L.q_active, L.d_active, L.status);
+        active_kernel<<<L.nq, 256, 0, stream>>>(L.d_scores, L.ld_ds, L.nd, L.q_off, L.qmap, L.q_active, L.d_active,
+                                               L.status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
         compact_items_kernel<uint8_t><<<1, kCompactThreads, 0, stream>>>(L.d_active, L.nd, L.d_list, L.d_count,
                                                                          L.status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
-        dd_zero_kernel<<<L.nd, 512, 0, stream>>>(L);
+    } else {
+        qmap_kernel<<<(L.nq + 255) / 256, 256, 0, stream>>>(L.q_off, L.nq, L.qmap, L.status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     const unsigned dq_grid = (L.rows_q + kDqRows - 1) / kDqRows;
