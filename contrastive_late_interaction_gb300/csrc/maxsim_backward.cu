@@ -76,8 +76,6 @@ template <int NBLK>   // 64-feature blocks of the width (1..4)
 // Up to width 128, at most 64 registers, so four blocks (32 warps) share an SM: the gathers are
 // latency-bound.
 __global__ void __launch_bounds__(256, NBLK <= 2 ? 4 : 2) dq_kernel(MaxSimBwdLaunch L) {
-    // dD (launched next) reads nothing dQ writes: let its CTAs start on the SMs this grid's last CTAs leave.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (read_status(L.status) != 0) return;
     const int t = blockIdx.x * kDqRows + (threadIdx.x >> 3);
     const int sub = threadIdx.x & 7;
@@ -294,6 +292,8 @@ __device__ __forceinline__ void dd_row_sum(const MaxSimBwdLaunch &L, const uint3
 template <int NB, int kDsUnroll>
 __global__ void __launch_bounds__(kDsThreads, 1) dd_sort_kernel(MaxSimBwdLaunch L) {
     extern __shared__ uint8_t ds_raw[];
+    // dQ (launched next) reads nothing dD writes: let its CTAs start on the SMs this grid's last wave leaves.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     uint32_t *cnt = reinterpret_cast<uint32_t *>(ds_raw);            // [kDsMaxRows] counts, then cursors
     uint32_t *off = cnt + kDsMaxRows;                                  // [kDsMaxRows + 1] bucket starts
     uint32_t *list = off + kDsMaxRows + 1;                             // [kDsChunk] (q << 16) | row offset
@@ -487,18 +487,18 @@ __global__ void __launch_bounds__(256) named_backward_kernel(MaxSimBwdLaunch L, 
 
 }  // namespace ms
 
-// dD as a programmatic dependent of the dQ grid launched just before it on the
-// same stream: its CTAs may start once every dQ CTA has started (dQ signals at
-// its start), filling the SMs that dQ's last wave leaves idle.  dD reads only
-// what the kernels before dQ wrote (they completed before dQ began), never
-// dQ's output, so it needs no wait on the dQ grid; the stream's later work
-// still waits for both.
+// dQ as a programmatic dependent of the dD grid launched just before it on the
+// same stream: its CTAs may start once every dD CTA has started (dD signals at
+// its start), filling the SMs that dD's last wave (one long CTA per SM, one
+// document each) leaves idle.  dQ reads only what the kernels before dD wrote
+// (they completed before dD began), never dD's output, so it needs no wait on
+// the dD grid; the stream's later work still waits for both.
 template <typename K>
-cudaError_t launch_after_dq(K kernel, const MaxSimBwdLaunch &L, size_t smem, cudaStream_t stream) {
+cudaError_t launch_after_dd(K kernel, const MaxSimBwdLaunch &L, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(L.nd));
-    cfg.blockDim = dim3(ms::kDsThreads);
-    cfg.dynamicSmemBytes = smem;
+    cfg.gridDim = dim3(static_cast<unsigned>((L.rows_q + ms::kDqRows - 1) / ms::kDqRows));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -525,25 +525,24 @@ cudaError_t launch_maxsim_backward(const MaxSimBwdLaunch &L, cudaStream_t stream
         qmap_kernel<<<(L.nq + 255) / 256, 256, 0, stream>>>(L.q_off, L.nq, L.qmap, L.status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
-    const unsigned dq_grid = (L.rows_q + kDqRows - 1) / kDqRows;
-    switch ((L.width + 63) / 64) {
-        case 1: dq_kernel<1><<<dq_grid, 256, 0, stream>>>(L); break;
-        case 2: dq_kernel<2><<<dq_grid, 256, 0, stream>>>(L); break;
-        case 3: dq_kernel<3><<<dq_grid, 256, 0, stream>>>(L); break;
-        default: dq_kernel<4><<<dq_grid, 256, 0, stream>>>(L); break;
-    }
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
     const size_t ds_smem = ds_smem_bytes();
     if ((L.width + 127) / 128 == 1) {
         if ((err = cudaFuncSetAttribute(dd_sort_kernel<1, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(ds_smem))) != cudaSuccess)
             return err;
-        err = launch_after_dq(dd_sort_kernel<1, 4>, L, ds_smem, stream);
+        dd_sort_kernel<1, 4><<<L.nd, kDsThreads, ds_smem, stream>>>(L);
     } else {
         if ((err = cudaFuncSetAttribute(dd_sort_kernel<2, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(ds_smem))) != cudaSuccess)
             return err;
-        err = launch_after_dq(dd_sort_kernel<2, 1>, L, ds_smem, stream);
+        dd_sort_kernel<2, 1><<<L.nd, kDsThreads, ds_smem, stream>>>(L);
+    }
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    switch ((L.width + 63) / 64) {
+        case 1: err = launch_after_dd(dq_kernel<1>, L, stream); break;
+        case 2: err = launch_after_dd(dq_kernel<2>, L, stream); break;
+        case 3: err = launch_after_dd(dq_kernel<3>, L, stream); break;
+        default: err = launch_after_dd(dq_kernel<4>, L, stream); break;
     }
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
