@@ -8,7 +8,9 @@
 // query row (8 threads per row, document resolutions shared by shuffles), and
 // dD sorts each document's query rows by their argmax target in shared memory
 // (histogram, scan, scatter) and then sums each target's bucket.  Queries and
-// documents no pair with c != 0 reaches are flagged first and skipped.
+// documents no pair with c != 0 reaches are flagged first and skipped.  dD runs
+// first; dQ, which reads nothing dD writes, is its programmatic dependent and
+// starts on the SMs that dD's last wave leaves.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -38,6 +40,8 @@ __global__ void active_kernel(const float *d_scores, long long ld_ds, int nd, co
     if (__syncthreads_or(any) && threadIdx.x == 0) q_active[q] = 1;
 }
 
+// The map from query row to query, when there are no activity flags to compute
+// (active_kernel writes it otherwise).
 __global__ void qmap_kernel(const uint64_t *q_off, int nq, int32_t *qmap, const int32_t *status) {
     if (read_status(status) != 0) return;
     const int q = blockIdx.x * blockDim.x + threadIdx.x;
